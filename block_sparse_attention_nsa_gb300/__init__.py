@@ -1,0 +1,248 @@
+"""Python binding of libnsa_sel.so: NSA selected attention on GB300 (sm_103a).
+
+Argument marshalling only.  Every step of the computation runs in the library's
+CUDA kernels; PyTorch provides device memory (outputs and workspace) and the
+current stream.  There is no CPU or PyTorch fallback: if the library is missing
+or a call fails, an exception is raised.
+
+Names follow the C ABI in include/nsa_sel_attn.h:
+  workspace_size, index, index_view, fwd, bwd, step_host, get_status,
+  profile_enable, profile_collect.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = ["Dims", "NsaError", "load", "workspace_size", "index", "index_view", "fwd", "bwd",
+           "staging_size", "step_host", "get_status", "profile_enable", "profile_collect",
+           "kernel_names", "make_dims", "LIB_PATH"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnsa_sel.so")
+
+NSA_BF16, NSA_FP16 = 0, 1
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
+           3: "workspace too small", 4: "CUDA error", 5: "bad index", 6: "timeout"}
+
+
+class NsaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {_STATUS.get(code, code)} (status {code})")
+        self.code = code
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+                ("h_q", ctypes.c_int32), ("h_k", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load():
+    """Load the in-tree library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} not found: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+    dp = ctypes.POINTER(Dims)
+    st = ctypes.c_int
+    sig = {
+        "nsa_sel_attn_workspace_size": (st, [dp, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
+        "nsa_sel_attn_index": (st, [dp, vp, vp, vp, sz, vp]),
+        "nsa_sel_attn_index_view": (st, [dp, vp, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                         ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                         ctypes.POINTER(vp), ctypes.POINTER(i32)]),
+        "nsa_sel_attn_fwd": (st, [dp, vp, vp, vp, vp, vp, f32, vp, vp, vp, sz, vp]),
+        "nsa_sel_attn_bwd": (st, [dp, vp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, sz,
+                                  ctypes.c_int, vp]),
+        "nsa_sel_attn_staging_size": (st, [dp, ctypes.POINTER(sz)]),
+        "nsa_sel_attn_step_host": (st, [dp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp, vp,
+                                        sz, vp, sz, vp]),
+        "nsa_sel_attn_get_status": (st, [dp, vp, vp, ctypes.POINTER(i32)]),
+        "nsa_sel_attn_num_kernels": (i32, []),
+        "nsa_sel_attn_kernel_name": (ctypes.c_char_p, [i32]),
+        "nsa_sel_attn_profile_enable": (st, [i32]),
+        "nsa_sel_attn_profile_collect": (st, [ctypes.POINTER(i32), ctypes.POINTER(f32)]),
+        "nsa_status_string": (ctypes.c_char_p, [st]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise NsaError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_dims(num_seqs: int, total_tokens: int, h_q: int, h_k: int, head_dim: int,
+              block_size: int, topk: int, dtype: torch.dtype) -> Dims:
+    code = {torch.bfloat16: NSA_BF16, torch.float16: NSA_FP16}.get(dtype)
+    if code is None:
+        raise NsaError(2, f"dtype {dtype}")
+    return Dims(num_seqs, total_tokens, h_q, h_k, head_dim, block_size, topk, code)
+
+
+def _dims_of(q, k, sel_idx, cu_seqlens, block_size) -> Dims:
+    if q.dim() != 3 or k.dim() != 3 or sel_idx.dim() != 3:
+        raise ValueError("q [N, h_q, d], k [N, h_k, d], sel_idx [h_k, N, T] expected")
+    return make_dims(cu_seqlens.numel() - 1, q.shape[0], q.shape[1], k.shape[1], q.shape[2],
+                     block_size, sel_idx.shape[2], q.dtype)
+
+
+def workspace_size(dims: Dims):
+    f, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().nsa_sel_attn_workspace_size(ctypes.byref(dims), ctypes.byref(f),
+                                              ctypes.byref(b)), "workspace_size")
+    return f.value, b.value
+
+
+def alloc_workspace(dims: Dims, device=None) -> torch.Tensor:
+    f, b = workspace_size(dims)
+    return torch.empty(max(f, b, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+
+
+def index(sel_idx, cu_seqlens, block_size, dims: Dims, workspace: torch.Tensor, stream=None):
+    _contig(sel_idx, cu_seqlens)
+    _check(load().nsa_sel_attn_index(ctypes.byref(dims), _ptr(sel_idx), _ptr(cu_seqlens),
+                                     _ptr(workspace), workspace.numel(), _stream(stream)), "index")
+
+
+def index_view(dims: Dims, workspace: torch.Tensor):
+    """Copies of the index tensors (synchronises): counts, offsets, q_list, slot_map, nb."""
+    ptrs = [ctypes.c_void_p() for _ in range(5)]
+    nbmax = ctypes.c_int32()
+    _check(load().nsa_sel_attn_index_view(ctypes.byref(dims), _ptr(workspace),
+                                          *[ctypes.byref(p) for p in ptrs],
+                                          ctypes.byref(nbmax)), "index_view")
+    base = workspace.data_ptr()
+
+    def view(ptr, count):
+        off = ptr.value - base
+        return workspace[off:off + 4 * count].view(torch.int32)
+
+    torch.cuda.synchronize()
+    nb = int(view(ptrs[4], 1).item())
+    nseg = dims.h_k * nb
+    counts = view(ptrs[0], nseg).clone()
+    offsets = view(ptrs[1], nseg + 1).clone()
+    total = int(offsets[-1].item()) if nseg > 0 else 0
+    q_list = view(ptrs[2], total).clone()
+    slot_map = view(ptrs[3], dims.h_k * dims.total_tokens * dims.topk).clone().view(
+        dims.h_k, dims.total_tokens, dims.topk)
+    return {"counts": counts, "offsets": offsets, "q_list": q_list, "slot_map": slot_map,
+            "num_blocks": nb}
+
+
+def fwd(q, k, v, sel_idx, cu_seqlens, block_size: int, scale: float,
+        workspace: Optional[torch.Tensor] = None, out=None, lse=None, stream=None):
+    """out [N, h_q, d] (q's dtype) and lse float32 [h_q, N]."""
+    _contig(q, k, v, sel_idx, cu_seqlens)
+    dims = _dims_of(q, k, sel_idx, cu_seqlens, block_size)
+    if workspace is None:
+        workspace = alloc_workspace(dims, q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    _check(load().nsa_sel_attn_fwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(sel_idx),
+                                   _ptr(cu_seqlens), float(scale), _ptr(out), _ptr(lse),
+                                   _ptr(workspace), workspace.numel(), _stream(stream)), "fwd")
+    return out, lse
+
+
+def bwd(q, k, v, sel_idx, cu_seqlens, block_size: int, scale: float, out, lse, dout,
+        workspace: Optional[torch.Tensor] = None, index_ready: bool = False, dq=None, dk=None,
+        dv=None, stream=None):
+    """dq, dk, dv (q's dtype).  index_ready reuses the index left in `workspace` by fwd."""
+    _contig(q, k, v, sel_idx, cu_seqlens, out, lse, dout)
+    dims = _dims_of(q, k, sel_idx, cu_seqlens, block_size)
+    if workspace is None:
+        workspace = alloc_workspace(dims, q.device)
+        index_ready = False
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(load().nsa_sel_attn_bwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(sel_idx),
+                                   _ptr(cu_seqlens), float(scale), _ptr(out), _ptr(lse),
+                                   _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                   workspace.numel(), 1 if index_ready else 0, _stream(stream)),
+           "bwd")
+    return dq, dk, dv
+
+
+def staging_size(dims: Dims) -> int:
+    n = ctypes.c_size_t()
+    _check(load().nsa_sel_attn_staging_size(ctypes.byref(dims), ctypes.byref(n)), "staging_size")
+    return n.value
+
+
+def step_host(dims: Dims, host: dict, scale: float, staging: torch.Tensor,
+              workspace: torch.Tensor, stream=None):
+    """Forward + backward from host (ideally pinned) tensors; results land in host tensors.
+
+    host: q, k, v, dout, sel_idx, cu_seqlens (inputs) and out, lse, dq, dk, dv (outputs).
+    """
+    _check(load().nsa_sel_attn_step_host(
+        ctypes.byref(dims), _ptr(host["q"]), _ptr(host["k"]), _ptr(host["v"]),
+        _ptr(host["sel_idx"]), _ptr(host["cu_seqlens"]), _ptr(host["dout"]), float(scale),
+        _ptr(host["out"]), _ptr(host.get("lse")), _ptr(host["dq"]), _ptr(host["dk"]),
+        _ptr(host["dv"]), _ptr(staging), staging.numel(), _ptr(workspace), workspace.numel(),
+        _stream(stream)), "step_host")
+
+
+def get_status(dims: Dims, workspace: torch.Tensor, stream=None):
+    """(status code, raw device bits); synchronises the stream and clears the word."""
+    bits = ctypes.c_int32()
+    code = load().nsa_sel_attn_get_status(ctypes.byref(dims), _ptr(workspace), _stream(stream),
+                                          ctypes.byref(bits))
+    return int(code), int(bits.value)
+
+
+def kernel_names():
+    lib = load()
+    return [lib.nsa_sel_attn_kernel_name(i).decode() for i in range(lib.nsa_sel_attn_num_kernels())]
+
+
+def profile_enable(on: bool = True):
+    _check(load().nsa_sel_attn_profile_enable(1 if on else 0), "profile_enable")
+
+
+def profile_collect():
+    """{kernel name: (launches, total ms)} since the last collect (synchronises)."""
+    lib = load()
+    n = lib.nsa_sel_attn_num_kernels()
+    launches = (ctypes.c_int32 * n)()
+    ms = (ctypes.c_float * n)()
+    _check(lib.nsa_sel_attn_profile_collect(launches, ms), "profile_collect")
+    return {name: (int(launches[i]), float(ms[i])) for i, name in enumerate(kernel_names())}

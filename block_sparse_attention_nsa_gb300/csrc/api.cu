@@ -1,0 +1,456 @@
+// api.cu -- the C ABI (include/nsa_sel_attn.h): argument validation, workspace
+// layout, kernel launches and the optional per-kernel event timing.
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "common.cuh"
+
+namespace nsa {
+cudaError_t launch_index(const Params &p, cudaStream_t s, void (*mark)(int, cudaStream_t, bool));
+cudaError_t index_set_smem_limits(size_t smem);
+cudaError_t launch_fwd(const Params &p, int num_sms, int64_t max_tiles, cudaStream_t s,
+                       void (*mark)(int, cudaStream_t, bool));
+cudaError_t launch_bwd(const Params &p, int num_sms, int64_t max_chunks, cudaStream_t s,
+                       void (*mark)(int, cudaStream_t, bool));
+
+namespace {
+
+constexpr int kNumKernels = 11;
+const char *const kKernelNames[kNumKernels] = {
+    "index_geometry", "index_count", "index_col_scan", "index_scan", "index_scatter",
+    "fwd_main", "fwd_merge", "bwd_preprocess", "bwd_main", "bwd_dq_reduce", "bwd_dkv_reduce"};
+
+// ---- per-kernel event timing (diagnostics; single host thread) ----
+struct Rec {
+  int id;
+  cudaEvent_t a, b;
+};
+struct Profiler {
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  std::vector<Rec> recs;
+  size_t used = 0;
+  cudaEvent_t pending = nullptr;
+  int pending_id = -1;
+  cudaEvent_t get() {
+    if (used == pool.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      pool.push_back(e);
+    }
+    return pool[used++];
+  }
+} g_prof;
+
+void mark(int id, cudaStream_t stream, bool begin) {
+  if (!g_prof.on) return;
+  cudaEvent_t e = g_prof.get();
+  if (!e) return;
+  cudaEventRecord(e, stream);
+  if (begin) {
+    g_prof.pending = e;
+    g_prof.pending_id = id;
+  } else if (g_prof.pending && g_prof.pending_id == id) {
+    g_prof.recs.push_back({id, g_prof.pending, e});
+    g_prof.pending = nullptr;
+  }
+}
+
+int num_sms_cached() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+nsa_status check_dims(const nsa_sel_attn_dims *d, bool bwd) {
+  if (!d) return NSA_ERR_INVALID_ARG;
+  if (d->num_seqs < 1 || d->total_tokens < 0 || d->h_k < 1 || d->h_q < 1 || d->topk < 1)
+    return NSA_ERR_INVALID_ARG;
+  if (d->h_q % d->h_k != 0) return NSA_ERR_INVALID_ARG;
+  if (d->dtype != NSA_BF16 && d->dtype != NSA_FP16) return NSA_ERR_UNSUPPORTED;
+  if (!(d->head_dim == 64 || d->head_dim == 128 || d->head_dim == 256)) return NSA_ERR_UNSUPPORTED;
+  if (bwd && d->head_dim != 128) return NSA_ERR_UNSUPPORTED;
+  if (!(d->block_size == 32 || d->block_size == 64 || d->block_size == 128))
+    return NSA_ERR_UNSUPPORTED;
+  if (d->topk > 32) return NSA_ERR_UNSUPPORTED;
+  const int64_t pairs = (int64_t)d->h_k * d->total_tokens * d->topk;
+  const int64_t g = d->h_q / d->h_k;
+  if (pairs >= (int64_t(1) << 31) || pairs * g >= (int64_t(1) << 31)) return NSA_ERR_UNSUPPORTED;
+  if ((int64_t)d->total_tokens * d->h_q >= (int64_t(1) << 31)) return NSA_ERR_UNSUPPORTED;
+  return NSA_OK;
+}
+
+nsa_status make_layout(const nsa_sel_attn_dims *d, Layout *L) {
+  const int64_t N = d->total_tokens, B = d->block_size, S = d->num_seqs, T = d->topk;
+  const int64_t g = d->h_q / d->h_k, h_k = d->h_k;
+  L->nb_max = (N + B - 1) / B + S;
+  L->max_pairs = h_k * N * T;
+  L->max_rows = L->max_pairs * g;
+  L->max_tiles = (L->max_rows + kTileRows - 1) / kTileRows + h_k * L->nb_max;
+  L->max_chunks = (L->max_tiles + kBwdChunkTiles - 1) / kBwdChunkTiles + h_k * L->nb_max;
+  int w = kIdxWarps;
+  const int64_t smem_cap = 200 * 1024;
+  while (w > 1 && (int64_t)w * L->nb_max * 4 > smem_cap) w >>= 1;
+  if ((int64_t)w * L->nb_max * 4 > smem_cap) return NSA_ERR_UNSUPPORTED;
+  L->idx_warps = w;
+  L->n_idx_tiles = (N + 32 * w - 1) / (32 * w);
+  if (L->n_idx_tiles < 1) L->n_idx_tiles = 1;
+  if (L->max_tiles >= (int64_t(1) << 31)) return NSA_ERR_UNSUPPORTED;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  const size_t nseg1 = static_cast<size_t>(h_k * L->nb_max + 1);
+  L->status = take(256);
+  L->nb = take(4);
+  L->blk_start = take(4 * static_cast<size_t>(S + 1));
+  L->counts = take(4 * nseg1);
+  L->offsets = take(4 * nseg1);
+  L->tile_off = take(4 * nseg1);
+  L->chunk_off = take(4 * nseg1);
+  L->q_list = take(4 * static_cast<size_t>(L->max_pairs > 0 ? L->max_pairs : 1));
+  L->slot_map = take(4 * static_cast<size_t>(h_k * N * T > 0 ? h_k * N * T : 1));
+  L->chunk_hist = take(4 * static_cast<size_t>(h_k * L->n_idx_tiles * L->nb_max));
+  L->index_end = o;
+  const size_t scratch = o;
+  L->obuf = take(static_cast<size_t>(L->max_rows) * d->head_dim * 2);
+  L->mlbuf = take(static_cast<size_t>(L->max_rows) * 8);
+  L->fwd_end = o;
+  o = scratch;
+  L->dstat = take(4 * static_cast<size_t>(N) * d->h_q);
+  L->dqbuf = take(static_cast<size_t>(L->max_rows) * d->head_dim * 2);
+  L->dkvbuf = take(static_cast<size_t>(L->max_chunks) * 2 * B * d->head_dim * 4);
+  L->bwd_end = o;
+  return NSA_OK;
+}
+
+void fill_params(Params *p, const nsa_sel_attn_dims *d, const Layout &L, void *ws) {
+  std::memset(p, 0, sizeof(*p));
+  p->num_seqs = d->num_seqs;
+  p->n = d->total_tokens;
+  p->h_q = d->h_q;
+  p->h_k = d->h_k;
+  p->g = d->h_q / d->h_k;
+  p->d = d->head_dim;
+  p->block = d->block_size;
+  p->topk = d->topk;
+  p->dtype = d->dtype;
+  char *w = static_cast<char *>(ws);
+  p->status = reinterpret_cast<int32_t *>(w + L.status);
+  p->nb = reinterpret_cast<int32_t *>(w + L.nb);
+  p->blk_start = reinterpret_cast<int32_t *>(w + L.blk_start);
+  p->counts = reinterpret_cast<int32_t *>(w + L.counts);
+  p->offsets = reinterpret_cast<int32_t *>(w + L.offsets);
+  p->tile_off = reinterpret_cast<int32_t *>(w + L.tile_off);
+  p->chunk_off = reinterpret_cast<int32_t *>(w + L.chunk_off);
+  p->q_list = reinterpret_cast<int32_t *>(w + L.q_list);
+  p->slot_map = reinterpret_cast<int32_t *>(w + L.slot_map);
+  p->chunk_hist = reinterpret_cast<int32_t *>(w + L.chunk_hist);
+  p->nb_max = L.nb_max;
+  p->n_idx_tiles = L.n_idx_tiles;
+  p->idx_warps = L.idx_warps;
+  p->obuf = w + L.obuf;
+  p->mlbuf = reinterpret_cast<float2 *>(w + L.mlbuf);
+  p->dstat = reinterpret_cast<float *>(w + L.dstat);
+  p->dqbuf = w + L.dqbuf;
+  p->dkvbuf = reinterpret_cast<float *>(w + L.dkvbuf);
+}
+
+nsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NSA_OK : NSA_ERR_CUDA; }
+
+nsa_status run_index(const nsa_sel_attn_dims *d, const Layout &L, Params &p, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(p.status, 0, 4, s);
+  if (e != cudaSuccess) return NSA_ERR_CUDA;
+  e = index_set_smem_limits(sizeof(int32_t) * L.idx_warps * L.nb_max);
+  if (e != cudaSuccess) return NSA_ERR_CUDA;
+  (void)d;
+  return cuda_status(launch_index(p, s, mark));
+}
+
+}  // namespace
+}  // namespace nsa
+
+using namespace nsa;
+
+extern "C" {
+
+nsa_status nsa_sel_attn_workspace_size(const nsa_sel_attn_dims *dims, size_t *fwd_bytes,
+                                       size_t *bwd_bytes) {
+  nsa_status st = check_dims(dims, false);
+  if (st != NSA_OK) return st;
+  Layout L;
+  st = make_layout(dims, &L);
+  if (st != NSA_OK) return st;
+  if (fwd_bytes) *fwd_bytes = L.fwd_end;
+  if (bwd_bytes) *bwd_bytes = L.bwd_end;
+  return NSA_OK;
+}
+
+nsa_status nsa_sel_attn_index(const nsa_sel_attn_dims *dims, const int32_t *sel_idx,
+                              const int32_t *cu_seqlens, void *workspace, size_t workspace_bytes,
+                              nsa_stream_t stream) {
+  nsa_status st = check_dims(dims, false);
+  if (st != NSA_OK) return st;
+  if (!cu_seqlens || !workspace || (dims->total_tokens > 0 && !sel_idx)) return NSA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return NSA_ERR_INVALID_ARG;
+  Layout L;
+  st = make_layout(dims, &L);
+  if (st != NSA_OK) return st;
+  if (workspace_bytes < L.index_end) return NSA_ERR_WORKSPACE;
+  Params p;
+  fill_params(&p, dims, L, workspace);
+  p.sel = sel_idx;
+  p.cu = cu_seqlens;
+  return run_index(dims, L, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nsa_status nsa_sel_attn_index_view(const nsa_sel_attn_dims *dims, const void *workspace,
+                                   const int32_t **counts, const int32_t **offsets,
+                                   const int32_t **q_list, const int32_t **slot_map,
+                                   const int32_t **nb_device, int32_t *num_blocks) {
+  nsa_status st = check_dims(dims, false);
+  if (st != NSA_OK) return st;
+  if (!workspace) return NSA_ERR_INVALID_ARG;
+  Layout L;
+  st = make_layout(dims, &L);
+  if (st != NSA_OK) return st;
+  const char *w = static_cast<const char *>(workspace);
+  if (counts) *counts = reinterpret_cast<const int32_t *>(w + L.counts);
+  if (offsets) *offsets = reinterpret_cast<const int32_t *>(w + L.offsets);
+  if (q_list) *q_list = reinterpret_cast<const int32_t *>(w + L.q_list);
+  if (slot_map) *slot_map = reinterpret_cast<const int32_t *>(w + L.slot_map);
+  if (nb_device) *nb_device = reinterpret_cast<const int32_t *>(w + L.nb);
+  if (num_blocks) *num_blocks = static_cast<int32_t>(L.nb_max);
+  return NSA_OK;
+}
+
+nsa_status nsa_sel_attn_fwd(const nsa_sel_attn_dims *dims, const void *q, const void *k,
+                            const void *v, const int32_t *sel_idx, const int32_t *cu_seqlens,
+                            float scale, void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, nsa_stream_t stream) {
+  nsa_status st = check_dims(dims, false);
+  if (st != NSA_OK) return st;
+  if (!cu_seqlens || !workspace || !std::isfinite(scale)) return NSA_ERR_INVALID_ARG;
+  if (dims->total_tokens > 0 && (!q || !k || !v || !sel_idx || !out || !lse))
+    return NSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 256))
+    return NSA_ERR_INVALID_ARG;
+  Layout L;
+  st = make_layout(dims, &L);
+  if (st != NSA_OK) return st;
+  if (workspace_bytes < L.fwd_end) return NSA_ERR_WORKSPACE;
+  if (dims->total_tokens == 0) return NSA_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Params p;
+  fill_params(&p, dims, L, workspace);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.sel = sel_idx;
+  p.cu = cu_seqlens;
+  p.out = out;
+  p.lse = lse;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  st = run_index(dims, L, p, s);
+  if (st != NSA_OK) return st;
+  return cuda_status(launch_fwd(p, num_sms_cached(), L.max_tiles, s, mark));
+}
+
+nsa_status nsa_sel_attn_bwd(const nsa_sel_attn_dims *dims, const void *q, const void *k,
+                            const void *v, const int32_t *sel_idx, const int32_t *cu_seqlens,
+                            float scale, const void *out, const float *lse, const void *dout,
+                            void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                            int index_ready, nsa_stream_t stream) {
+  nsa_status st = check_dims(dims, true);
+  if (st != NSA_OK) return st;
+  if (!cu_seqlens || !workspace || !std::isfinite(scale)) return NSA_ERR_INVALID_ARG;
+  if (dims->total_tokens > 0 &&
+      (!q || !k || !v || !sel_idx || !out || !lse || !dout || !dq || !dk || !dv))
+    return NSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 256))
+    return NSA_ERR_INVALID_ARG;
+  Layout L;
+  st = make_layout(dims, &L);
+  if (st != NSA_OK) return st;
+  if (workspace_bytes < L.bwd_end) return NSA_ERR_WORKSPACE;
+  if (dims->total_tokens == 0) return NSA_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Params p;
+  fill_params(&p, dims, L, workspace);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.sel = sel_idx;
+  p.cu = cu_seqlens;
+  p.out_in = out;
+  p.lse_in = lse;
+  p.dout = dout;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  if (!index_ready) {
+    st = run_index(dims, L, p, s);
+    if (st != NSA_OK) return st;
+  }
+  return cuda_status(launch_bwd(p, num_sms_cached(), L.max_chunks, s, mark));
+}
+
+nsa_status nsa_sel_attn_staging_size(const nsa_sel_attn_dims *dims, size_t *bytes) {
+  nsa_status st = check_dims(dims, false);
+  if (st != NSA_OK) return st;
+  if (!bytes) return NSA_ERR_INVALID_ARG;
+  const size_t N = dims->total_tokens, d = dims->head_dim;
+  const size_t qb = align256(N * dims->h_q * d * 2), kb = align256(N * dims->h_k * d * 2);
+  const size_t selb = align256(4 * N * dims->h_k * dims->topk);
+  const size_t cub = align256(4 * static_cast<size_t>(dims->num_seqs + 1));
+  const size_t lseb = align256(4 * N * dims->h_q);
+  // q, k, v, dout, sel, cu, out, lse, dq, dk, dv
+  *bytes = 3 * qb + 4 * kb + selb + cub + lseb + qb;
+  return NSA_OK;
+}
+
+nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const void *host_q,
+                                  const void *host_k, const void *host_v,
+                                  const int32_t *host_sel_idx, const int32_t *host_cu_seqlens,
+                                  const void *host_dout, float scale, void *host_out,
+                                  float *host_lse, void *host_dq, void *host_dk, void *host_dv,
+                                  void *staging, size_t staging_bytes, void *workspace,
+                                  size_t workspace_bytes, nsa_stream_t stream) {
+  nsa_status st = check_dims(dims, true);
+  if (st != NSA_OK) return st;
+  size_t need = 0;
+  nsa_sel_attn_staging_size(dims, &need);
+  if (!staging || staging_bytes < need || !aligned(staging, 256)) return NSA_ERR_INVALID_ARG;
+  if (!host_cu_seqlens) return NSA_ERR_INVALID_ARG;
+  const size_t N = dims->total_tokens, d = dims->head_dim;
+  if (N > 0 && (!host_q || !host_k || !host_v || !host_sel_idx || !host_dout || !host_out ||
+                !host_dq || !host_dk || !host_dv))
+    return NSA_ERR_INVALID_ARG;
+  const size_t qbytes = N * dims->h_q * d * 2, kbytes = N * dims->h_k * d * 2;
+  const size_t selbytes = 4 * N * dims->h_k * dims->topk;
+  const size_t cubytes = 4 * static_cast<size_t>(dims->num_seqs + 1), lsebytes = 4 * N * dims->h_q;
+  char *w = static_cast<char *>(staging);
+  size_t o = 0;
+  auto take = [&](size_t b) {
+    char *at = w + o;
+    o += align256(b);
+    return at;
+  };
+  char *q = take(qbytes), *k = take(kbytes), *v = take(kbytes), *dout = take(qbytes);
+  char *sel = take(selbytes), *cu = take(cubytes), *out = take(qbytes);
+  char *lse = take(lsebytes), *dq = take(qbytes), *dk = take(kbytes), *dv = take(kbytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const struct { void *dst; const void *src; size_t n; } h2d[] = {
+      {q, host_q, qbytes}, {k, host_k, kbytes}, {v, host_v, kbytes}, {dout, host_dout, qbytes},
+      {sel, host_sel_idx, selbytes}, {cu, host_cu_seqlens, cubytes}};
+  for (const auto &c : h2d)
+    if (c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return NSA_ERR_CUDA;
+  st = nsa_sel_attn_fwd(dims, q, k, v, reinterpret_cast<int32_t *>(sel),
+                        reinterpret_cast<int32_t *>(cu), scale, out, reinterpret_cast<float *>(lse),
+                        workspace, workspace_bytes, stream);
+  if (st != NSA_OK) return st;
+  st = nsa_sel_attn_bwd(dims, q, k, v, reinterpret_cast<int32_t *>(sel),
+                        reinterpret_cast<int32_t *>(cu), scale, out, reinterpret_cast<float *>(lse),
+                        dout, dq, dk, dv, workspace, workspace_bytes, 1, stream);
+  if (st != NSA_OK) return st;
+  const struct { void *dst; const void *src; size_t n; } d2h[] = {
+      {host_out, out, qbytes}, {host_lse, lse, host_lse ? lsebytes : 0}, {host_dq, dq, qbytes},
+      {host_dk, dk, kbytes}, {host_dv, dv, kbytes}};
+  for (const auto &c : d2h)
+    if (c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return NSA_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(s));
+}
+
+nsa_status nsa_sel_attn_get_status(const nsa_sel_attn_dims *dims, void *workspace,
+                                   nsa_stream_t stream, int32_t *bits) {
+  nsa_status st = check_dims(dims, false);
+  if (st != NSA_OK) return st;
+  if (!workspace) return NSA_ERR_INVALID_ARG;
+  Layout L;
+  st = make_layout(dims, &L);
+  if (st != NSA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t word = 0;
+  char *w = static_cast<char *>(workspace);
+  if (cudaMemcpyAsync(&word, w + L.status, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return NSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NSA_ERR_CUDA;
+  if (cudaMemsetAsync(w + L.status, 0, 4, s) != cudaSuccess) return NSA_ERR_CUDA;
+  if (bits) *bits = word;
+  if (word & NSA_DEVERR_TIMEOUT) return NSA_ERR_TIMEOUT;
+  if (word & (NSA_DEVERR_BAD_INDEX | NSA_DEVERR_BAD_SEQLENS)) return NSA_ERR_BAD_INDEX;
+  return NSA_OK;
+}
+
+int32_t nsa_sel_attn_num_kernels(void) { return kNumKernels; }
+
+const char *nsa_sel_attn_kernel_name(int32_t id) {
+  return (id >= 0 && id < kNumKernels) ? kKernelNames[id] : "unknown";
+}
+
+nsa_status nsa_sel_attn_profile_enable(int32_t on) {
+  g_prof.on = on != 0;
+  return NSA_OK;
+}
+
+nsa_status nsa_sel_attn_profile_collect(int32_t *launches, float *total_ms) {
+  if (!launches || !total_ms) return NSA_ERR_INVALID_ARG;
+  for (int i = 0; i < kNumKernels; ++i) {
+    launches[i] = 0;
+    total_ms[i] = 0.f;
+  }
+  nsa_status st = NSA_OK;
+  for (const Rec &r : g_prof.recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) {
+      st = NSA_ERR_CUDA;
+      continue;
+    }
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+      st = NSA_ERR_CUDA;
+      continue;
+    }
+    launches[r.id] += 1;
+    total_ms[r.id] += ms;
+  }
+  g_prof.recs.clear();
+  g_prof.used = 0;
+  g_prof.pending = nullptr;
+  return st;
+}
+
+const char *nsa_status_string(nsa_status status) {
+  switch (status) {
+    case NSA_OK: return "ok";
+    case NSA_ERR_INVALID_ARG: return "invalid argument";
+    case NSA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case NSA_ERR_WORKSPACE: return "workspace too small";
+    case NSA_ERR_CUDA: return "CUDA error";
+    case NSA_ERR_BAD_INDEX: return "invalid selection index or sequence offsets seen on device";
+    case NSA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

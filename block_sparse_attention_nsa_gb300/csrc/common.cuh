@@ -1,0 +1,302 @@
+// common.cuh -- shared definitions of the sm_103a selected-attention kernels:
+// parameter blocks, workspace layout and thin inline-PTX wrappers for the
+// Blackwell primitives used (tcgen05 MMA / TMEM, mbarrier, cp.async).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nsa_sel_attn.h"
+
+namespace nsa {
+
+// ---------------------------------------------------------------------------
+// Tiling constants
+// ---------------------------------------------------------------------------
+constexpr int kTileRows = 128;      // gathered (token, query head) rows per MMA tile (tcgen05 M)
+constexpr int kBwdChunkTiles = 8;   // backward: row tiles one CTA accumulates dK/dV over
+constexpr int kIdxWarps = 8;        // index builder: warps per token tile (32 tokens each)
+constexpr int kThreads = 128;       // main kernels: one thread per tile row / TMEM lane
+
+// ---------------------------------------------------------------------------
+// Workspace layout (byte offsets from the workspace base, all 256-aligned)
+// ---------------------------------------------------------------------------
+struct Layout {
+  int64_t nb_max;          // upper bound on blocks per head: ceil(N/B_K) + S
+  int64_t max_pairs;       // upper bound on kept (token, slot) pairs: h_k * N * T
+  int64_t max_rows;        // max_pairs * g
+  int64_t max_tiles;       // upper bound on 128-row tiles over all segments
+  int64_t max_chunks;      // upper bound on backward chunks
+  int64_t n_idx_tiles;     // token tiles of the index builder
+  int idx_warps;           // warps per index tile (bounded by shared memory)
+  // index region
+  size_t status, nb, blk_start, counts, offsets, tile_off, chunk_off, q_list, slot_map,
+      chunk_hist;
+  size_t index_end;
+  // forward scratch
+  size_t obuf, mlbuf;
+  size_t fwd_end;
+  // backward scratch
+  size_t dstat, dqbuf, dkvbuf;
+  size_t bwd_end;
+};
+
+// ---------------------------------------------------------------------------
+// Kernel parameter block (shared by all kernels; plain pointers + sizes)
+// ---------------------------------------------------------------------------
+struct Params {
+  // problem
+  int32_t num_seqs, n, h_q, h_k, g, d, block, topk, dtype;
+  float scale, scale_log2;
+  // inputs
+  const void *q, *k, *v, *out_in, *dout;
+  const float *lse_in;
+  const int32_t *sel, *cu;
+  // outputs
+  void *out, *dq, *dk, *dv;
+  float *lse;
+  // workspace views
+  int32_t *status, *nb, *blk_start, *counts, *offsets, *tile_off, *chunk_off, *q_list,
+      *slot_map, *chunk_hist;
+  int64_t nb_max, n_idx_tiles;
+  int idx_warps;
+  void *obuf;       // forward partial outputs [rows, d] (dtype)
+  float2 *mlbuf;    // forward partial (max, sum) per row, log2 domain
+  float *dstat;     // backward D = rowsum(dO * O) [h_q, N]
+  void *dqbuf;      // backward partial dQ [rows, d] (dtype)
+  float *dkvbuf;    // backward per-chunk dK, dV partials [chunks, 2, B_K, d] fp32
+};
+
+// ---------------------------------------------------------------------------
+// Small device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void set_status(int32_t *status, int32_t bits) {
+  atomicOr(reinterpret_cast<int *>(status), bits);
+}
+
+// Largest s in [0, S) with cu[s] <= t (cu non-decreasing).
+__device__ __forceinline__ int seq_of(const int32_t *cu, int num_seqs, int t) {
+  int lo = 0, hi = num_seqs - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Largest i in [0, n) with a[i] <= x (a non-decreasing, a[0] <= x).
+__device__ __forceinline__ int upper_index(const int32_t *a, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (a[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier (bounded waits: give up after ~2 s and report NSA_DEVERR_TIMEOUT)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Returns false (and flags the status word) when the phase did not complete in time.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *status) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(addr, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      set_status(status, NSA_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// cp.async (16-byte global -> shared copies; src_bytes = 0 zero-fills)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+// Generic-proxy shared-memory writes -> visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory tiles in the 128-byte-swizzled layout used by tcgen05 operands.
+// A tile of R rows x C 16-bit columns is stored as C/64 "column blocks"; column
+// block cb holds, for each row r, 128 bytes (64 elements) at cb*R*128 + r*128,
+// with its eight 16-byte chunks permuted chunk -> chunk ^ (r % 8).  Tile bases are
+// 1024-byte aligned.  The same storage serves as a K-major operand (rows = M or N,
+// columns = K) or as an MN-major operand (rows = K, columns = M or N).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk, int rows) {
+  // chunk = 16-byte chunk index along the full row (8 chunks per column block)
+  return static_cast<uint32_t>((chunk >> 3) * rows * 128 + row * 128 +
+                               (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+// tcgen05 shared-memory matrix descriptor, 128-byte swizzle, sm_100 family version.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t desc = 0;
+  desc |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  desc |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  desc |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  desc |= static_cast<uint64_t>(1) << 46;   // descriptor version (tcgen05)
+  desc |= static_cast<uint64_t>(2) << 61;   // 128-byte swizzle
+  return desc;
+}
+
+// K-major operand: rows are the M (or N) dimension, columns the K dimension.
+// k-step s covers columns [16 s, 16 s + 16).
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int rows, int s) {
+  return sdesc_sw128(tile + (s >> 2) * rows * 128 + (s & 3) * 32, 16, 1024);
+}
+
+// MN-major operand: rows are the K dimension, columns the M (or N) dimension.
+// k-step s covers rows [16 s, 16 s + 16); the next 64 M/N columns are one column
+// block (rows * 128 bytes) further.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int rows, int s) {
+  return sdesc_sw128(tile + s * 2048, rows * 128, 1024);
+}
+
+// Instruction descriptor, kind::f16: D = f32, A/B = bf16 (or f16), dense.
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool a_mn, bool b_mn, bool fp16) {
+  return (1u << 4) | ((fp16 ? 0u : 1u) << 7) | ((fp16 ? 0u : 1u) << 10) |
+         ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05: TMEM allocation, MMA, commit, loads
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T  (one elected thread issues)
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once all previously issued tcgen05.mma of this thread complete.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 consecutive fp32 TMEM columns of this thread's lane, waited on before returning.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------------------
+// dtype helpers (bf16 / fp16 stored as raw 16-bit)
+// ---------------------------------------------------------------------------
+template <bool kFp16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (kFp16) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+}
+template <bool kFp16>
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+  if constexpr (kFp16) {
+    __half2 h = *reinterpret_cast<__half2 *>(&u);
+    return __half22float2(h);
+  } else {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&u);
+    return __bfloat1622float2(h);
+  }
+}
+template <bool kFp16>
+__device__ __forceinline__ float round16(float x) {
+  if constexpr (kFp16) return __half2float(__float2half_rn(x));
+  else return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+}  // namespace nsa

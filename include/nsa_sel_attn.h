@@ -1,0 +1,174 @@
+/*
+ * nsa_sel_attn.h -- C ABI of the GB300 (sm_103a) selected-attention library.
+ *
+ * Native Sparse Attention's selected-attention (token-selection) branch: every
+ * query token of a GQA group attends, causally, only to the T KV blocks of B_K
+ * keys that the selection tensor names for it, with one softmax over the union
+ * of those keys ("FSA: An Alternative Efficient Implementation of Native Sparse
+ * Attention Kernel", key designs 1-4; Flash-Sparse-Attention README, "Method").
+ *
+ * Conventions for every entry point
+ *   - Pointers named q, k, v, out, lse, dout, dq, dk, dv, sel_idx, cu_seqlens and
+ *     workspace are DEVICE pointers unless the name says host_.  The caller owns
+ *     every buffer and the stream; the library allocates no device memory.
+ *   - Calls are asynchronous on `stream` and never synchronise it, except
+ *     nsa_sel_attn_get_status, nsa_sel_attn_profile_collect and the host-buffer
+ *     entry nsa_sel_attn_step_host, which say so.
+ *   - Arguments are validated before anything is enqueued; a failing check
+ *     returns an error and writes nothing.  A CUDA launch error is returned as
+ *     NSA_ERR_CUDA.  Nothing aborts or exits.
+ *   - Layouts (all contiguous, row-major; packed variable-length batch of S
+ *     sequences concatenated along tokens, N = cu_seqlens[S]):
+ *       q, out, dout, dq   [N, h_q, head_dim]   (dtype)
+ *       k, v, dk, dv       [N, h_k, head_dim]   (dtype)
+ *       sel_idx            int32 [h_k, N, topk] block indices local to the token's sequence
+ *       cu_seqlens         int32 [S + 1], cu_seqlens[0] = 0, non-decreasing
+ *       lse                float32 [h_q, N], natural log, softmax scale included
+ *     Query head hq uses KV head hq / (h_q / h_k).  q/k/v/out/dout/dq/dk/dv must be
+ *     16-byte aligned; the workspace 256-byte aligned.
+ *   - Selection semantics: for token t at position tau of its sequence, slot value b
+ *     counts when 0 <= b <= tau / B_K (causal) and b < ceil(len / B_K); -1 marks an
+ *     empty slot; duplicates count once; keys b*B_K + i > tau are masked.  Values
+ *     below -1 or past the sequence's last block are skipped and also raise the
+ *     NSA_DEVERR_BAD_INDEX bit of the device status word.  A token with no valid
+ *     block gets out = 0 and lse = -inf.
+ *   - Supported envelope: dtype bf16 or fp16; head_dim in {64, 128, 256}
+ *     (backward: 128); block_size in {32, 64, 128}; 1 <= topk <= 32;
+ *     h_q a multiple of h_k; h_k * N * topk < 2^31.  Anything else returns
+ *     NSA_ERR_UNSUPPORTED.
+ */
+#ifndef NSA_SEL_ATTN_H
+#define NSA_SEL_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NSA_API __attribute__((visibility("default")))
+#else
+#define NSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *nsa_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    NSA_OK = 0,
+    NSA_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, misaligned buffer */
+    NSA_ERR_UNSUPPORTED = 2,   /* outside the supported envelope above */
+    NSA_ERR_WORKSPACE = 3,     /* workspace smaller than nsa_sel_attn_workspace_size */
+    NSA_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    NSA_ERR_BAD_INDEX = 5,     /* nsa_sel_attn_get_status: device saw invalid sel_idx/cu_seqlens */
+    NSA_ERR_TIMEOUT = 6        /* nsa_sel_attn_get_status: a bounded device wait gave up */
+} nsa_status;
+
+typedef enum { NSA_BF16 = 0, NSA_FP16 = 1 } nsa_dtype;
+
+/* Bits of the device status word (read by nsa_sel_attn_get_status). */
+enum {
+    NSA_DEVERR_BAD_INDEX = 1,     /* sel_idx value < -1 or past the sequence's last block */
+    NSA_DEVERR_BAD_SEQLENS = 2,   /* cu_seqlens not starting at 0 / decreasing / not ending at N */
+    NSA_DEVERR_TIMEOUT = 4        /* an mbarrier wait hit its iteration limit */
+};
+
+typedef struct {
+    int32_t num_seqs;      /* S >= 1 */
+    int32_t total_tokens;  /* N = cu_seqlens[S] (checked on the device) */
+    int32_t h_q;           /* query heads */
+    int32_t h_k;           /* KV heads; g = h_q / h_k query heads share one KV head */
+    int32_t head_dim;      /* d, same for q, k and v */
+    int32_t block_size;    /* B_K, keys per KV block */
+    int32_t topk;          /* T, slots per (KV head, token) in sel_idx */
+    int32_t dtype;         /* nsa_dtype of q, k, v, out, dout, dq, dk, dv */
+} nsa_sel_attn_dims;
+
+/* Workspace bytes for nsa_sel_attn_fwd and nsa_sel_attn_bwd (host only, no CUDA
+ * call).  Both start with the same index region, so one buffer of
+ * max(fwd_bytes, bwd_bytes) serves a forward followed by a backward that reuses
+ * the forward's index (index_ready = 1).  Either output pointer may be NULL. */
+NSA_API nsa_status nsa_sel_attn_workspace_size(const nsa_sel_attn_dims *dims, size_t *fwd_bytes,
+                                       size_t *bwd_bytes);
+
+/* Index tensors of key design 2 (histogram, exclusive scan, scatter), built into
+ * the workspace's index region: counts[h*NB + gb] tokens selected global block gb
+ * (gb = local block + blocks of earlier sequences, NB = sum_s ceil(len_s / B_K));
+ * offsets = exclusive scan (KV-head major), offsets[h_k*NB] = number of pairs;
+ * q_list[offsets[i] + r] = the r-th token, ascending, that selected block i (I_i);
+ * slot_map[h, t, k] = position of that (token, slot) pair, -1 when not kept (O_i).
+ * nsa_sel_attn_fwd calls this itself; it is exported for tests and for a backward
+ * without a forward. */
+NSA_API nsa_status nsa_sel_attn_index(const nsa_sel_attn_dims *dims, const int32_t *sel_idx,
+                              const int32_t *cu_seqlens, void *workspace, size_t workspace_bytes,
+                              nsa_stream_t stream);
+
+/* Device pointers into the workspace's index region (host only, no CUDA call).
+ * num_blocks receives the host upper bound NB_max used for the layout; the true
+ * NB is written on the device at *nb_device.  Any output pointer may be NULL. */
+NSA_API nsa_status nsa_sel_attn_index_view(const nsa_sel_attn_dims *dims, const void *workspace,
+                                   const int32_t **counts, const int32_t **offsets,
+                                   const int32_t **q_list, const int32_t **slot_map,
+                                   const int32_t **nb_device, int32_t *num_blocks);
+
+/* Forward: out (dtype) and lse (float32) from q, k, v and the selection.
+ * Builds the index, then runs the per-KV-block main kernel (gathered query rows x
+ * one KV block on tcgen05 tensor cores, partial outputs with their own softmax
+ * max and sum written to a compact buffer) and the merge kernel that combines the
+ * partials of every (token, query head) with log-sum-exp weights (the statistics
+ * and reduction stages of key designs 3-4). */
+NSA_API nsa_status nsa_sel_attn_fwd(const nsa_sel_attn_dims *dims, const void *q, const void *k,
+                            const void *v, const int32_t *sel_idx, const int32_t *cu_seqlens,
+                            float scale, void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, nsa_stream_t stream);
+
+/* Backward: dq, dk, dv (dtype) from q, k, v, the forward's out and lse, and dout.
+ * index_ready = 1 reuses the index that nsa_sel_attn_fwd (or _index) left in this
+ * workspace (the backward reuses the forward's I_i / O_i, key design 2);
+ * index_ready = 0 rebuilds it.  dk and dv are fully overwritten. */
+NSA_API nsa_status nsa_sel_attn_bwd(const nsa_sel_attn_dims *dims, const void *q, const void *k,
+                            const void *v, const int32_t *sel_idx, const int32_t *cu_seqlens,
+                            float scale, const void *out, const float *lse, const void *dout,
+                            void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                            int index_ready, nsa_stream_t stream);
+
+/* Device staging bytes for nsa_sel_attn_step_host (host only). */
+NSA_API nsa_status nsa_sel_attn_staging_size(const nsa_sel_attn_dims *dims, size_t *bytes);
+
+/* One training step of the branch from HOST buffers: copies q, k, v, dout,
+ * sel_idx and cu_seqlens to the caller's device staging buffer, runs forward and
+ * backward (reusing the index), copies out, lse, dq, dk and dv back to the host
+ * buffers, and synchronises the stream.  Host buffers should be pinned for the
+ * copies to be asynchronous.  host_lse may be NULL to skip that copy. */
+NSA_API nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const void *host_q,
+                                  const void *host_k, const void *host_v,
+                                  const int32_t *host_sel_idx, const int32_t *host_cu_seqlens,
+                                  const void *host_dout, float scale, void *host_out,
+                                  float *host_lse, void *host_dq, void *host_dk, void *host_dv,
+                                  void *staging, size_t staging_bytes, void *workspace,
+                                  size_t workspace_bytes, nsa_stream_t stream);
+
+/* Synchronises `stream`, reads and clears the device status word of this
+ * workspace.  Returns NSA_OK, NSA_ERR_BAD_INDEX or NSA_ERR_TIMEOUT (the worst
+ * seen) and stores the raw bits in *bits when bits is not NULL. */
+NSA_API nsa_status nsa_sel_attn_get_status(const nsa_sel_attn_dims *dims, void *workspace,
+                                   nsa_stream_t stream, int32_t *bits);
+
+/* Kernel timing for diagnostics.  While enabled, every kernel the library
+ * launches is bracketed by CUDA events on its launch stream (the library creates
+ * and owns the events).  collect synchronises on them and adds, per kernel id,
+ * the launch count and total milliseconds since the last collect; arrays have
+ * nsa_sel_attn_num_kernels() entries. */
+NSA_API int32_t nsa_sel_attn_num_kernels(void);
+NSA_API const char *nsa_sel_attn_kernel_name(int32_t id);
+NSA_API nsa_status nsa_sel_attn_profile_enable(int32_t on);
+NSA_API nsa_status nsa_sel_attn_profile_collect(int32_t *launches, float *total_ms);
+
+NSA_API const char *nsa_status_string(nsa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NSA_SEL_ATTN_H */

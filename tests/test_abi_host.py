@@ -1,0 +1,97 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every
+symbol declared in include/*.h, sizes workspaces, and rejects bad arguments
+before enqueueing anything."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_attention_nsa_gb300 import build
+    build.build()
+    import block_sparse_attention_nsa_gb300 as nsa
+    return nsa.load()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names |= set(re.findall(r"NSA_API\s+[\w\s\*]+?\b(nsa_\w+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert len(declared) >= 10
+    so = os.path.join(ROOT, "block_sparse_attention_nsa_gb300", "libnsa_sel.so")
+    out = subprocess.run(["nm", "-D", "--defined-only", so], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (nsa_\w+)", out))
+    assert declared <= exported, declared - exported
+    for name in declared:
+        assert getattr(lib, name) is not None
+
+
+def _dims(**kw):
+    import block_sparse_attention_nsa_gb300 as nsa
+    base = dict(num_seqs=1, total_tokens=8192, h_q=4, h_k=4, head_dim=128, block_size=64,
+                topk=16, dtype=0)
+    base.update(kw)
+    return nsa.Dims(**base)
+
+
+def test_workspace_size_and_envelope(lib):
+    import block_sparse_attention_nsa_gb300 as nsa
+    f, b = nsa.workspace_size(_dims())
+    assert f > 0 and b > 0
+    # compact partial buffer bound: h_k * N * T rows of d 16-bit values
+    assert f >= 4 * 8192 * 16 * 128 * 2
+    bad = [dict(head_dim=96), dict(block_size=48), dict(topk=33), dict(dtype=7), dict(h_q=6),
+           dict(h_k=0), dict(num_seqs=0), dict(total_tokens=-1)]
+    for kw in bad:
+        with pytest.raises(nsa.NsaError):
+            nsa.workspace_size(_dims(**kw))
+    # too many pairs for 32-bit positions
+    with pytest.raises(nsa.NsaError) as e:
+        nsa.workspace_size(_dims(total_tokens=1 << 27, topk=32))
+    assert e.value.code == 2
+
+
+def test_validation_returns_before_launch(lib):
+    d = _dims()
+    fake = ctypes.c_void_p(1 << 20)      # never dereferenced: every call below fails validation
+    st = lib.nsa_sel_attn_fwd(ctypes.byref(d), fake, fake, fake, fake, fake, 0.1, fake, fake,
+                              fake, 16, None)
+    assert st == 3                       # workspace too small
+    st = lib.nsa_sel_attn_fwd(ctypes.byref(d), None, fake, fake, fake, fake, 0.1, fake, fake,
+                              fake, 1 << 40, None)
+    assert st == 1                       # null q
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    st = lib.nsa_sel_attn_fwd(ctypes.byref(d), odd, fake, fake, fake, fake, 0.1, fake, fake,
+                              fake, 1 << 40, None)
+    assert st == 1                       # q not 16-byte aligned
+    st = lib.nsa_sel_attn_fwd(ctypes.byref(d), fake, fake, fake, fake, fake, float("nan"), fake,
+                              fake, fake, 1 << 40, None)
+    assert st == 1                       # non-finite scale
+    d256 = _dims(head_dim=256)
+    st = lib.nsa_sel_attn_bwd(ctypes.byref(d256), fake, fake, fake, fake, fake, 0.1, fake, fake,
+                              fake, fake, fake, fake, fake, 1 << 40, 0, None)
+    assert st == 2                       # backward envelope is d <= 128
+    st = lib.nsa_sel_attn_index(None, fake, fake, fake, 1 << 40, None)
+    assert st == 1
+
+
+def test_status_strings_and_kernel_names(lib):
+    import block_sparse_attention_nsa_gb300 as nsa
+    for code in range(7):
+        assert lib.nsa_status_string(code)
+    names = nsa.kernel_names()
+    assert "fwd_main" in names and "index_scatter" in names and "bwd_main" in names

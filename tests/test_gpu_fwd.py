@@ -1,0 +1,103 @@
+"""GPU forward vs the fp64 oracle on the same seeded inputs (through the C ABI).
+
+Small workloads are compared element by element; the 64K and varlen workloads
+at full size, in the launch configuration the benchmark times, on sampled
+(token, query head) rows that the oracle computes one by one."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import check_forward, sample_rows, to_device
+from workloads import CONFIGS, WorkloadConfig, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(cfg, inp):
+    import block_sparse_attention_nsa_gb300 as nsa
+    dv = to_device(inp)
+    out, lse = nsa.fwd(dv["q"], dv["k"], dv["v"], dv["sel_idx"], dv["cu_seqlens"], cfg.block,
+                       cfg.scale)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+@pytest.mark.parametrize("name", ["tiny", "fwd8k"])
+def test_forward_full_compare(name):
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg)
+    out, lse = _run(cfg, inp)
+    ref_out, ref_lse = oracle.fwd(inp["cu_seqlens"], cfg.block, inp["sel_idx"], inp["q"],
+                                  inp["k"], inp["v"], cfg.scale)
+    check_forward(out, lse, ref_out, ref_lse, name)
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_forward_64k_sampled(g):
+    cfg = CONFIGS["fwd64k"].with_g(g)
+    inp = make_inputs(cfg)
+    out, lse = _run(cfg, inp)
+    rows = sample_rows(cfg.n, cfg.h_q, 3000, seed=g, block=cfg.block)
+    ref_o, ref_l = oracle.fwd_rows(inp["cu_seqlens"], cfg.block, inp["sel_idx"], inp["q"],
+                                   inp["k"], inp["v"], cfg.scale, rows)
+    o = out[rows[:, 0], rows[:, 1]]
+    l = lse[rows[:, 1], rows[:, 0]]
+    check_forward(o, l, ref_o, ref_l, cfg.name)
+
+
+def test_forward_varlen_sampled():
+    cfg = CONFIGS["varlen"]
+    inp = make_inputs(cfg)
+    out, lse = _run(cfg, inp)
+    rows = sample_rows(cfg.n, cfg.h_q, 3000, seed=7, seqlens=list(cfg.seqlens), block=cfg.block)
+    ref_o, ref_l = oracle.fwd_rows(inp["cu_seqlens"], cfg.block, inp["sel_idx"], inp["q"],
+                                   inp["k"], inp["v"], cfg.scale, rows)
+    check_forward(out[rows[:, 0], rows[:, 1]], lse[rows[:, 1], rows[:, 0]], ref_o, ref_l,
+                  "varlen")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("block", [32, 64, 128])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_forward_shapes_ragged(d, block, dtype):
+    # several sequences with ragged tails, small T, g = 3 (rows not a multiple of 128)
+    cfg = WorkloadConfig("ragged", (300, 1, 517, 64, 0, 250), 2, 3, d, block, 5, dtype,
+                         "uniform", 1.0, 77)
+    inp = make_inputs(cfg)
+    out, lse = _run(cfg, inp)
+    ref_out, ref_lse = oracle.fwd(inp["cu_seqlens"], cfg.block, inp["sel_idx"], inp["q"],
+                                  inp["k"], inp["v"], cfg.scale)
+    check_forward(out, lse, ref_out, ref_lse, f"d{d} B{block} {dtype}")
+
+
+def test_forward_degenerate_selections():
+    # rows with no valid block (-1 only, future blocks only), duplicates, T = 1 and T = 32
+    for topk in (1, 32):
+        cfg = WorkloadConfig("degen", (700, 129), 1, 2, 128, 64, topk, "bf16", "uniform", 1.0,
+                             11 + topk)
+        inp = make_inputs(cfg)
+        sel = inp["sel_idx"]
+        sel[0, 100, :] = -1
+        sel[0, 5, 0] = 3                           # future block only
+        sel[0, 600, :] = sel[0, 600, :1]           # all slots the same block
+        out, lse = _run(cfg, inp)
+        ref_out, ref_lse = oracle.fwd(inp["cu_seqlens"], cfg.block, sel, inp["q"], inp["k"],
+                                      inp["v"], cfg.scale)
+        check_forward(out, lse, ref_out, ref_lse, f"T={topk}")
+        assert torch.all(out[100] == 0) and torch.isinf(lse[:, 100]).all()
+
+
+def test_forward_dense_special_case_matches_sdpa():
+    # every causal block selected: the kernel must equal dense causal attention
+    n, block = 512, 64
+    cfg = WorkloadConfig("dense", (n,), 2, 2, 128, block, n // block, "bf16", "uniform", 1.0, 3)
+    inp = make_inputs(cfg)
+    sel = np.full((2, n, n // block), -1, dtype=np.int32)
+    for t in range(n):
+        sel[:, t, : t // block + 1] = np.arange(t // block + 1)[::-1]
+    inp["sel_idx"] = sel
+    out, lse = _run(cfg, inp)
+    ref_out, ref_lse = oracle.fwd(inp["cu_seqlens"], block, sel, inp["q"], inp["k"], inp["v"],
+                                  cfg.scale)
+    check_forward(out, lse, ref_out, ref_lse, "dense")
