@@ -149,6 +149,30 @@ NSA_API nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const v
                                   void *staging, size_t staging_bytes, void *workspace,
                                   size_t workspace_bytes, nsa_stream_t stream);
 
+/* Size of the fixed scratch array used by nsa_sel_attn_fwd_noalloc (16 MiB). */
+#define NSA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* Forward without any device allocation, for callers that cannot allocate: code
+ * running during CUDA graph capture, plugins whose host framework owns all device
+ * memory, loops that cannot afford an allocation's synchronisation.  Same inputs,
+ * outputs and results as nsa_sel_attn_fwd, but the scratch is a fixed array of
+ * NSA_NOALLOC_SCRATCH_BYTES inside the library (held by every GPU that loads the
+ * library until exit).  The paper has no counterpart to this entry point.
+ *   - Problems whose forward workspace (nsa_sel_attn_workspace_size) exceeds
+ *     NSA_NOALLOC_SCRATCH_BYTES are rejected with NSA_ERR_WORKSPACE; nothing runs.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array and it keeps the last call's contents: calls
+ *     that may overlap on the GPU (different streams without ordering, several
+ *     host threads) race; serialise them.  The call clears the status word itself
+ *     and writes every scratch entry it reads, so no clearing is needed between
+ *     calls.  nsa_sel_attn_get_status does not apply to this scratch. */
+NSA_API nsa_status nsa_sel_attn_fwd_noalloc(const nsa_sel_attn_dims *dims, const void *q,
+                                            const void *k, const void *v, const int32_t *sel_idx,
+                                            const int32_t *cu_seqlens, float scale, void *out,
+                                            float *lse, nsa_stream_t stream);
+
 /* Synchronises `stream`, reads and clears the device status word of this
  * workspace.  Returns NSA_OK, NSA_ERR_BAD_INDEX or NSA_ERR_TIMEOUT (the worst
  * seen) and stores the raw bits in *bits when bits is not NULL. */
