@@ -40,6 +40,7 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true", help="skip the g = 1, 2, 4, 8 sweep")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     return ap.parse_args()
 
 
@@ -328,7 +329,7 @@ def run_ours(args, rank, world):
                 del rr
                 torch.cuda.empty_cache()
         result["sweep"] = sweep
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and not args.no_cpu and args.cpu_seconds > 0:
         result["cpu_baseline"] = cpu_baseline(cfg, r.host, args.cpu_seconds)
     return result
 
