@@ -147,6 +147,78 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
   }
 }
 
+// Waits used by warp-specialised kernels: once any wait of the CTA has timed out
+// (*fail set), every later wait returns at once, so all roles run their loops to
+// the end with unchanged control flow (no thread is left behind at a barrier).
+__device__ __forceinline__ bool mbar_wait_sticky(uint64_t *bar, uint32_t parity,
+                                                 int32_t *status, volatile int *fail) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (*fail) return false;
+    if (mbar_try_wait(addr, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *fail = 1;
+      set_status(status, NSA_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// TMA (tensor-map loads into 128-byte-swizzled tiles) and bulk stores
+// ---------------------------------------------------------------------------
+// 3-D tiled load; completion is counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Four rows (r0..r3) of a 2-D tensor map with a one-row box, columns [col, col + box).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int col, int r0,
+                                            int r1, int r2, int r3, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *gdst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // cp.async (16-byte global -> shared copies; src_bytes = 0 zero-fills)
 // ---------------------------------------------------------------------------
@@ -269,6 +341,51 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// ---------------------------------------------------------------------------
+// Walks the 128-row tiles of consecutive (KV head, block) segments in order.
+// set(t) moves to tile t (>= the previous one); `jseg` counts the distinct
+// segments visited so far (0 for the first), which indexes K/V buffer slots.
+// ---------------------------------------------------------------------------
+struct TileCursor {
+  int nb, nseg;
+  int seg, seg_first_tile, seg_end_tile;
+  int h, gb, key0, seg_off, seg_rows;
+  int row0, nrows, jseg;
+  bool new_seg;
+
+  __device__ __forceinline__ void load_seg(const Params &p) {
+    h = seg / nb;
+    gb = seg - h * nb;
+    const int s = upper_index(p.blk_start, p.num_seqs + 1, gb);
+    key0 = p.cu[s] + (gb - p.blk_start[s]) * p.block;
+    seg_off = p.offsets[seg];
+    seg_rows = (p.offsets[seg + 1] - seg_off) * p.g;
+    seg_first_tile = p.tile_off[seg];
+    seg_end_tile = p.tile_off[seg + 1];
+  }
+  __device__ __forceinline__ void start(const Params &p, int nb_, int tile0) {
+    nb = nb_;
+    nseg = p.h_k * nb_;
+    seg = upper_index(p.tile_off, nseg + 1, tile0);
+    load_seg(p);
+    jseg = -1;
+    new_seg = true;
+  }
+  // Tile `t` must be >= every tile passed before; the first call starts segment 0.
+  __device__ __forceinline__ void set(const Params &p, int t) {
+    bool moved = jseg < 0;
+    if (t >= seg_end_tile) {
+      while (p.tile_off[seg + 1] <= t) ++seg;
+      load_seg(p);
+      moved = true;
+    }
+    new_seg = moved;
+    if (moved) ++jseg;
+    row0 = (t - seg_first_tile) * 128;
+    nrows = min(128, seg_rows - row0);
+  }
+};
 
 // ---------------------------------------------------------------------------
 // dtype helpers (bf16 / fp16 stored as raw 16-bit)
