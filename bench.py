@@ -150,6 +150,12 @@ class Runner:
                      self.lse, self.dout, workspace=self.ws, index_ready=True, dq=self.dq,
                      dk=self.dk, dv=self.dv)
 
+    def bwd_rebuild(self):
+        c = self.cfg
+        self.nsa.bwd(self.q, self.k, self.v, self.sel, self.cu, c.block, c.scale, self.out,
+                     self.lse, self.dout, workspace=self.ws, index_ready=False, dq=self.dq,
+                     dk=self.dk, dv=self.dv)
+
     def step(self):
         self.fwd()
         self.bwd()
@@ -160,15 +166,23 @@ class Runner:
             raise RuntimeError(f"device status {code} (bits {bits})")
 
 
-def time_fn(torch, fn, iters):
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+def time_reps(torch, fn, reps):
+    """Per-call device times (ms) of `reps` back-to-back calls, CUDA events on the
+    current stream, synchronised before and after."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
     torch.cuda.synchronize()
-    s.record()
-    for _ in range(iters):
+    evs[0].record()
+    for i in range(reps):
         fn()
-    e.record()
+        evs[i + 1].record()
     torch.cuda.synchronize()
-    return s.elapsed_time(e) / iters
+    return [evs[i].elapsed_time(evs[i + 1]) for i in range(reps)]
+
+
+def dist(ms_list):
+    a = np.asarray(ms_list, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "reps": int(a.size)}
 
 
 def e2e_measure(r: Runner, iters: int):
@@ -239,36 +253,42 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     r.check_status()
 
+    # ---- headline: exactly K steps, the library's event profiler off ----
     if world > 1:
         torch.distributed.barrier()
     with ClockSampler(dev.index) as clk:
-        nsa.profile_enable(True)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record()
-        for _ in range(args.steps):
-            r.step()
-        ev1.record()
-        torch.cuda.synchronize()
+        step_ms = time_reps(torch, r.step, args.steps)
         if world > 1:
             torch.distributed.barrier()
-        nsa.profile_enable(False)
-    ms = ev0.elapsed_time(ev1) / args.steps
-    kern = nsa.profile_collect()
+    ms = float(np.sum(step_ms)) / args.steps
     r.check_status()
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
 
-    # separate forward / backward times (outside the headline region)
-    fwd_ms = time_fn(torch, r.fwd, max(3, args.steps // 2))
-    bwd_ms = time_fn(torch, r.bwd, max(3, args.steps // 2))
+    # ---- per-kernel split: a separate pass with the event profiler on ----
+    prof_steps = 3
+    nsa.profile_enable(True)
+    for _ in range(prof_steps):
+        r.step()
+    torch.cuda.synchronize()
+    nsa.profile_enable(False)
+    kern = nsa.profile_collect()
+    r.check_status()
+
+    # ---- forward / backward alone (outside the headline region) ----
+    reps = max(50, args.steps)
+    fwd_d = dist(time_reps(torch, r.fwd, reps))
+    bwd_d = dist(time_reps(torch, r.bwd, reps))
+    bwd0_d = dist(time_reps(torch, r.bwd_rebuild, max(10, reps // 5)))
+    fwd_ms, bwd_ms = fwd_d["median"], bwd_d["median"]
 
     pk_burst, pk_sust, hbm, pk_kind = peaks()
-    launches = sum(n for n, _ in kern.values())
+    launches = int(round(sum(n for n, _ in kern.values()) / prof_steps))
     dom = max(DOMINANT, key=lambda name: kern.get(name, (0, 0.0))[1])
     n_l, tot = kern[dom]
     per_launch_ms = tot / max(1, n_l)
@@ -298,7 +318,11 @@ def run_ours(args, rank, world):
         "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,
         "bwd_tflops": 2.5 * fwd_flops / (bwd_ms * 1e-3) / 1e12,
         "pct_bf16_peak_step": 100.0 * (step_flops / (ms * 1e-3) / 1e12) / pk_burst,
-        "kernels_ms_per_step": {k: t / args.steps for k, (n, t) in kern.items() if n},
+        "step_ms_dist": dist(step_ms),
+        "fwd_ms_dist": fwd_d, "bwd_ms_dist": bwd_d,
+        "bwd_rebuild_index_ms_dist": bwd0_d,
+        "kernels_ms_per_step": {k: t / prof_steps for k, (n, t) in kern.items() if n},
+        "kernels_sum_ms_per_step": step_tot / prof_steps,
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": pk_burst,
                      "unit": "TFLOP/s", "frac": achieved / pk_burst, "traffic": None,
                      "peak_kind": f"{pk_kind} bf16 burst",
@@ -319,8 +343,8 @@ def run_ours(args, rank, world):
             rr = r if g == cfg.g else Runner(c, c.seed, dev)
             ff = useful_fwd_flops(c)
             rr.step()
-            f_ms = time_fn(torch, rr.fwd, 5)
-            b_ms = time_fn(torch, rr.bwd, 5)
+            f_ms = dist(time_reps(torch, rr.fwd, 20))["median"]
+            b_ms = dist(time_reps(torch, rr.bwd, 20))["median"]
             sweep[f"g{g}"] = {"fwd_ms": f_ms, "bwd_ms": b_ms,
                               "fwd_tflops": ff / (f_ms * 1e-3) / 1e12,
                               "bwd_tflops": 2.5 * ff / (b_ms * 1e-3) / 1e12,

@@ -58,7 +58,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         list(ex.map(run, jobs))
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        run([_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-lcuda"])
+        run([_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"])
         os.replace(tmp, LIB)
     return LIB
 

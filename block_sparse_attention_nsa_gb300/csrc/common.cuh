@@ -71,6 +71,21 @@ struct Params {
 };
 
 // ---------------------------------------------------------------------------
+// Driver API entry points, resolved through the runtime at first use so that the
+// library does not link libcuda and loads on a machine without a GPU driver.
+// Returns nullptr when the driver (or the symbol) is missing.
+// ---------------------------------------------------------------------------
+template <typename Fn>
+inline Fn driver_entry(const char *name) {
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(fn);
+}
+
+// ---------------------------------------------------------------------------
 // Small device helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

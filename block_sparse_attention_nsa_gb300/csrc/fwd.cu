@@ -379,8 +379,14 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(Params p) {
 // ---------------------------------------------------------------------------
 static bool encode_map(CUtensorMap *map, bool fp16, int rank, const void *base,
                        const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box) {
+  using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static const EncodeFn encode = driver_entry<EncodeFn>("cuTensorMapEncodeTiled");
+  if (!encode) return false;
   const cuuint32_t elem[3] = {1, 1, 1};
-  return cuTensorMapEncodeTiled(map,
+  return encode(map,
                                 fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                 rank, const_cast<void *>(base), dims, strides, box, elem,

@@ -160,18 +160,29 @@ NSA_API nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const v
  * library until exit).  The paper has no counterpart to this entry point.
  *   - Problems whose forward workspace (nsa_sel_attn_workspace_size) exceeds
  *     NSA_NOALLOC_SCRATCH_BYTES are rejected with NSA_ERR_WORKSPACE; nothing runs.
- *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current); make that first call before any stream
- *     capture.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and keeps it; the lookup is repeated when the device's
+ *     current context has changed (after cudaDeviceReset, for instance).  Make the
+ *     first call in each context before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents: calls
  *     that may overlap on the GPU (different streams without ordering, several
  *     host threads) race; serialise them.  The call clears the status word itself
  *     and writes every scratch entry it reads, so no clearing is needed between
- *     calls.  nsa_sel_attn_get_status does not apply to this scratch. */
+ *     calls.  Device-side error bits of a call are read with
+ *     nsa_sel_attn_fwd_noalloc_status. */
 NSA_API nsa_status nsa_sel_attn_fwd_noalloc(const nsa_sel_attn_dims *dims, const void *q,
                                             const void *k, const void *v, const int32_t *sel_idx,
                                             const int32_t *cu_seqlens, float scale, void *out,
                                             float *lse, nsa_stream_t stream);
+
+/* Device status word of the fixed scratch used by nsa_sel_attn_fwd_noalloc: the
+ * same contract as nsa_sel_attn_get_status (synchronises `stream`, reads and
+ * clears the word, returns NSA_OK, NSA_ERR_BAD_INDEX or NSA_ERR_TIMEOUT and the raw
+ * bits).  dims must be those of the call being checked; the same size limit
+ * applies.  Like the entry point itself, it allocates nothing.  The paper has no
+ * counterpart to this function. */
+NSA_API nsa_status nsa_sel_attn_fwd_noalloc_status(const nsa_sel_attn_dims *dims,
+                                                   nsa_stream_t stream, int32_t *bits);
 
 /* Synchronises `stream`, reads and clears the device status word of this
  * workspace.  Returns NSA_OK, NSA_ERR_BAD_INDEX or NSA_ERR_TIMEOUT (the worst

@@ -12,8 +12,12 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-@pytest.fixture(scope="module")
-def lib():
+# Every test runs twice: once in the CPU tier and once, unchanged, in the GPU
+# tier, so the host-side contract is also checked on the machine that runs the
+# kernels (the library must load and validate identically with a driver present).
+@pytest.fixture(scope="module", params=[pytest.param("host"),
+                                        pytest.param("gpu-box", marks=pytest.mark.gpu)])
+def lib(request):
     from block_sparse_attention_nsa_gb300 import build
     build.build()
     import block_sparse_attention_nsa_gb300 as nsa
