@@ -8,7 +8,7 @@
 
 namespace nsa {
 cudaError_t launch_index(const Params &p, cudaStream_t s, void (*mark)(int, cudaStream_t, bool));
-cudaError_t index_set_smem_limits(size_t smem);
+cudaError_t index_set_smem_limits(const Params &p);
 cudaError_t launch_fwd(const Params &p, int num_sms, int64_t max_tiles, cudaStream_t s,
                        void (*mark)(int, cudaStream_t, bool));
 cudaError_t launch_bwd(const Params &p, int num_sms, int64_t max_chunks, cudaStream_t s,
@@ -18,7 +18,7 @@ namespace {
 
 constexpr int kNumKernels = 11;
 const char *const kKernelNames[kNumKernels] = {
-    "index_geometry", "index_count", "index_col_scan", "index_scan", "index_scatter",
+    "index_geometry", "index_count", "index_col_scan", "index_scans_and_tiles", "index_scatter",
     "fwd_main", "fwd_merge", "bwd_preprocess", "bwd_main", "bwd_dq_reduce", "bwd_dkv_reduce"};
 
 // ---- per-kernel event timing (diagnostics; single host thread) ----
@@ -91,6 +91,10 @@ nsa_status check_dims(const nsa_sel_attn_dims *d, bool bwd) {
   return NSA_OK;
 }
 
+// Shared memory the index builder may use per CTA (count: one int per block;
+// scatter: one bit per (token, block) of the CTA's token tile).
+constexpr int64_t kIdxSmemCap = 160 * 1024;
+
 nsa_status make_layout(const nsa_sel_attn_dims *d, Layout *L) {
   const int64_t N = d->total_tokens, B = d->block_size, S = d->num_seqs, T = d->topk;
   const int64_t g = d->h_q / d->h_k, h_k = d->h_k;
@@ -99,14 +103,22 @@ nsa_status make_layout(const nsa_sel_attn_dims *d, Layout *L) {
   L->max_rows = L->max_pairs * g;
   L->max_tiles = (L->max_rows + kTileRows - 1) / kTileRows + h_k * L->nb_max;
   L->max_chunks = (L->max_tiles + kBwdChunkTiles - 1) / kBwdChunkTiles + h_k * L->nb_max;
-  int w = kIdxWarps;
-  const int64_t smem_cap = 200 * 1024;
-  while (w > 1 && (int64_t)w * L->nb_max * 4 > smem_cap) w >>= 1;
-  if ((int64_t)w * L->nb_max * 4 > smem_cap) return NSA_ERR_UNSUPPORTED;
-  L->idx_warps = w;
-  L->n_idx_tiles = (N + 32 * w - 1) / (32 * w);
+  if (L->nb_max * 4 > kIdxSmemCap) return NSA_ERR_UNSUPPORTED;
+  int tok = kIdxThreads;
+  while (tok > 32 && (tok / 32) * L->nb_max * 4 > kIdxSmemCap) tok >>= 1;
+  if ((tok / 32) * L->nb_max * 4 > kIdxSmemCap) return NSA_ERR_UNSUPPORTED;
+  L->idx_tok = tok;
+  L->n_idx_tiles = (N + tok - 1) / tok;
   if (L->n_idx_tiles < 1) L->n_idx_tiles = 1;
-  if (L->max_tiles >= (int64_t(1) << 31)) return NSA_ERR_UNSUPPORTED;
+  // One wave over all tokens: sub-segments coincide with the (head, block) segments.
+  L->wave_tiles = static_cast<int>(L->n_idx_tiles);
+  L->n_w = 1;
+  L->nsub = h_k * L->n_w * L->nb_max;
+  L->max_wtiles = (L->max_rows + kTileRows - 1) / kTileRows + L->nsub;
+  L->n_scan_ctas = (L->nsub + kScanPer - 1) / kScanPer;
+  if (L->max_tiles >= (int64_t(1) << 31) / kTileRows ||
+      L->max_wtiles >= (int64_t(1) << 31) / kTileRows)
+    return NSA_ERR_UNSUPPORTED;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -114,6 +126,8 @@ nsa_status make_layout(const nsa_sel_attn_dims *d, Layout *L) {
     return at;
   };
   const size_t nseg1 = static_cast<size_t>(h_k * L->nb_max + 1);
+  const size_t hn = static_cast<size_t>(h_k * N > 0 ? h_k * N : 1);
+  const size_t hnt = static_cast<size_t>(h_k * N * T > 0 ? h_k * N * T : 1);
   L->status = take(256);
   L->nb = take(4);
   L->blk_start = take(4 * static_cast<size_t>(S + 1));
@@ -122,12 +136,18 @@ nsa_status make_layout(const nsa_sel_attn_dims *d, Layout *L) {
   L->tile_off = take(4 * nseg1);
   L->chunk_off = take(4 * nseg1);
   L->q_list = take(4 * static_cast<size_t>(L->max_pairs > 0 ? L->max_pairs : 1));
-  L->slot_map = take(4 * static_cast<size_t>(h_k * N * T > 0 ? h_k * N * T : 1));
+  L->slot_map = take(4 * hnt);
   L->chunk_hist = take(4 * static_cast<size_t>(h_k * L->n_idx_tiles * L->nb_max));
+  L->npairs = take(4 * hn);
+  L->cnt = take(4 * hn);
+  L->prow = take(4 * hnt);
+  L->wtile_off = take(4 * static_cast<size_t>(L->nsub + 1));
+  L->wscan_part = take(4 * static_cast<size_t>(L->n_scan_ctas));
+  L->tdesc = take(sizeof(TileDesc) * static_cast<size_t>(L->max_wtiles));
   L->index_end = o;
   const size_t scratch = o;
-  L->obuf = take(static_cast<size_t>(L->max_rows) * d->head_dim * 2);
-  L->mlbuf = take(static_cast<size_t>(L->max_rows) * 8);
+  L->obuf = take(static_cast<size_t>(L->max_wtiles) * kTileRows * d->head_dim * 2);
+  L->mlbuf = take(static_cast<size_t>(L->max_wtiles) * kTileRows * 8);
   L->fwd_end = o;
   o = scratch;
   L->dstat = take(4 * static_cast<size_t>(N) * d->h_q);
@@ -159,9 +179,20 @@ void fill_params(Params *p, const nsa_sel_attn_dims *d, const Layout &L, void *w
   p->q_list = reinterpret_cast<int32_t *>(w + L.q_list);
   p->slot_map = reinterpret_cast<int32_t *>(w + L.slot_map);
   p->chunk_hist = reinterpret_cast<int32_t *>(w + L.chunk_hist);
+  p->npairs = reinterpret_cast<int32_t *>(w + L.npairs);
+  p->cnt = reinterpret_cast<int32_t *>(w + L.cnt);
+  p->prow = reinterpret_cast<int32_t *>(w + L.prow);
+  p->wtile_off = reinterpret_cast<int32_t *>(w + L.wtile_off);
+  p->wscan_part = reinterpret_cast<int32_t *>(w + L.wscan_part);
+  p->tdesc = reinterpret_cast<TileDesc *>(w + L.tdesc);
   p->nb_max = L.nb_max;
   p->n_idx_tiles = L.n_idx_tiles;
-  p->idx_warps = L.idx_warps;
+  p->nsub = L.nsub;
+  p->n_scan_ctas = L.n_scan_ctas;
+  p->idx_tok = L.idx_tok;
+  p->n_w = L.n_w;
+  p->wave_tiles = L.wave_tiles;
+  p->fwd_chunk = 0;
   p->obuf = w + L.obuf;
   p->mlbuf = reinterpret_cast<float2 *>(w + L.mlbuf);
   p->dstat = reinterpret_cast<float *>(w + L.dstat);
@@ -174,7 +205,7 @@ nsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NSA_OK : NSA_E
 nsa_status run_index(const nsa_sel_attn_dims *d, const Layout &L, Params &p, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(p.status, 0, 4, s);
   if (e != cudaSuccess) return NSA_ERR_CUDA;
-  e = index_set_smem_limits(sizeof(int32_t) * L.idx_warps * L.nb_max);
+  e = index_set_smem_limits(p);
   if (e != cudaSuccess) return NSA_ERR_CUDA;
   (void)d;
   return cuda_status(launch_index(p, s, mark));
@@ -268,7 +299,7 @@ nsa_status nsa_sel_attn_fwd(const nsa_sel_attn_dims *dims, const void *q, const 
   p.scale_log2 = scale * 1.4426950408889634f;
   st = run_index(dims, L, p, s);
   if (st != NSA_OK) return st;
-  return cuda_status(launch_fwd(p, num_sms_cached(), L.max_tiles, s, mark));
+  return cuda_status(launch_fwd(p, num_sms_cached(), L.max_wtiles, s, mark));
 }
 
 nsa_status nsa_sel_attn_bwd(const nsa_sel_attn_dims *dims, const void *q, const void *k,

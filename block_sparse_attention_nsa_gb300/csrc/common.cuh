@@ -18,8 +18,9 @@ namespace nsa {
 // ---------------------------------------------------------------------------
 constexpr int kTileRows = 128;      // gathered (token, query head) rows per MMA tile (tcgen05 M)
 constexpr int kBwdChunkTiles = 8;   // backward: row tiles one CTA accumulates dK/dV over
-constexpr int kIdxWarps = 8;        // index builder: warps per token tile (32 tokens each)
-constexpr int kThreads = 128;       // main kernels: one thread per tile row / TMEM lane
+constexpr int kIdxThreads = 256;    // index builder: threads per CTA (one token per thread)
+constexpr int kThreads = 128;       // backward main kernel: one thread per tile row / TMEM lane
+constexpr int kScanPer = 4096;      // entries per CTA of the multi-CTA exclusive scan
 
 // ---------------------------------------------------------------------------
 // Workspace layout (byte offsets from the workspace base, all 256-aligned)
@@ -28,13 +29,18 @@ struct Layout {
   int64_t nb_max;          // upper bound on blocks per head: ceil(N/B_K) + S
   int64_t max_pairs;       // upper bound on kept (token, slot) pairs: h_k * N * T
   int64_t max_rows;        // max_pairs * g
-  int64_t max_tiles;       // upper bound on 128-row tiles over all segments
+  int64_t max_tiles;       // upper bound on 128-row tiles over the (head, block) segments
   int64_t max_chunks;      // upper bound on backward chunks
+  int idx_tok;             // tokens per index-builder CTA (256, 128, 64 or 32)
   int64_t n_idx_tiles;     // token tiles of the index builder
-  int idx_warps;           // warps per index tile (bounded by shared memory)
+  int n_w;                 // forward waves (token windows processed one after another)
+  int wave_tiles;          // index token tiles per forward wave
+  int64_t nsub;            // forward sub-segments: h_k * n_w * nb_max (head, wave, block)
+  int64_t max_wtiles;      // upper bound on forward tiles over the sub-segments
+  int64_t n_scan_ctas;     // CTAs of the sub-segment tile scan
   // index region
   size_t status, nb, blk_start, counts, offsets, tile_off, chunk_off, q_list, slot_map,
-      chunk_hist;
+      chunk_hist, npairs, cnt, prow, wtile_off, wscan_part, tdesc;
   size_t index_end;
   // forward scratch
   size_t obuf, mlbuf;
@@ -42,6 +48,15 @@ struct Layout {
   // backward scratch
   size_t dstat, dqbuf, dkvbuf;
   size_t bwd_end;
+};
+
+// Forward tile descriptor (one per 128-row tile of a (head, wave, block) sub-segment).
+//   q_off : q_list index of the sub-segment's first token
+//   row0  : first row of the tile inside the sub-segment (rows = token-major, g heads)
+//   key0  : global index of the block's first key
+//   hn    : KV head | (rows in this tile) << 16
+struct TileDesc {
+  int32_t q_off, row0, key0, hn;
 };
 
 // ---------------------------------------------------------------------------
@@ -60,11 +75,13 @@ struct Params {
   float *lse;
   // workspace views
   int32_t *status, *nb, *blk_start, *counts, *offsets, *tile_off, *chunk_off, *q_list,
-      *slot_map, *chunk_hist;
-  int64_t nb_max, n_idx_tiles;
-  int idx_warps;
-  void *obuf;       // forward partial outputs [rows, d] (dtype)
-  float2 *mlbuf;    // forward partial (max, sum) per row, log2 domain
+      *slot_map, *chunk_hist, *npairs, *cnt, *prow, *wtile_off, *wscan_part;
+  TileDesc *tdesc;
+  int64_t nb_max, n_idx_tiles, nsub, n_scan_ctas;
+  int idx_tok, n_w, wave_tiles;
+  int fwd_chunk;    // forward schedule: consecutive tiles per chunk, chunks dealt round-robin
+  void *obuf;       // forward partial outputs [tiles * 128, d] (dtype), tile-padded rows
+  float2 *mlbuf;    // forward partial (max, sum) per padded row, log2 domain
   float *dstat;     // backward D = rowsum(dO * O) [h_q, N]
   void *dqbuf;      // backward partial dQ [rows, d] (dtype)
   float *dkvbuf;    // backward per-chunk dK, dV partials [chunks, 2, B_K, d] fp32
@@ -248,6 +265,11 @@ __device__ __forceinline__ void cp_async_commit() {
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
+// Wait until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 // Generic-proxy shared-memory writes -> visible to the tensor core (async proxy).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -330,6 +352,19 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T: A is M x K with row m in TMEM lane m and two
+// 16-bit K elements per 32-bit column (element k of the row in column k / 2, low
+// half for even k).  Used for O += P V with P written to TMEM by the softmax.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on `bar` once all previously issued tcgen05.mma of this thread complete.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(
@@ -355,6 +390,34 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane (a warp writes its
+// 32-lane subpartition); the caller waits with tmem_wait_st before signalling.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 2-D tiled TMA store from a 128-byte-swizzled shared-memory box (bulk group).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int c0,
+                                             int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_le1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -1,17 +1,19 @@
 // fwd.cu -- forward of NSA selected attention on sm_103a.
 //
 // Loop order follows "FSA: An Alternative Efficient Implementation of Native
-// Sparse Attention Kernel" (key design 1): the outer loop is over (KV head, KV
-// block) segments of the index, the inner one over 128-row tiles of the query
-// rows (token, query head) that selected the block, so the MMA's M dimension is
-// filled by gathered queries and no GQA-group padding is needed.
+// Sparse Attention Kernel" (key design 1): the outer loop is over KV blocks, the
+// inner one over 128-row tiles of the query rows (token, query head) that selected
+// the block, so the MMA's M dimension is filled by gathered queries and no
+// GQA-group padding is needed.  Tiles come from (KV head, wave, block)
+// sub-segments of the index: a wave is a window of consecutive tokens, so the
+// rows of one wave are finished before the next wave starts.
 //
 //   fwd_main  : per tile, S = Q K_b^T (tcgen05, TMEM accumulator, M = 128,
-//               N = B_K), masked row max m and P = exp2(S*scale*log2e - m) in
-//               registers, O = P V_b (tcgen05, N = d).  The unnormalised partial
-//               O and its (m, l = fp32 sum of P) go to the compact buffer at the pair's
-//               position (O_i of key design 2), so a tile's output is one
-//               contiguous block of memory.
+//               N = B_K); masked row max m and P = exp2(S*scale*log2e - m) in
+//               registers, P written back to TMEM in 16 bits; O = P V_b (tcgen05
+//               with A = P read from TMEM, N = d).  The unnormalised partial O of
+//               every row and its (m, l = fp32 sum of P) go to the compact buffer
+//               (key design 2), one 128-row block per tile, by TMA tensor stores.
 //   fwd_merge : per (token, query head), the <= T partials are combined with
 //               log-sum-exp weights into out and lse.  Carrying (m, l) with each
 //               partial replaces the separate statistics kernel of key design 4:
@@ -26,83 +28,115 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Pipeline depths per (d, B_K), bounded by 227 KB of shared memory and 512 TMEM
-// columns: Q stages (a Q stage also stages the tile's 16-bit output), K/V stages,
-// P buffers, O accumulators (TMEM).
+// Pipeline depths per (d, B_K), bounded by 227 KB of shared memory: Q stages and
+// K/V stages.  Two output staging slots (one per softmax warpgroup) of one
+// 64-column block each.  TMEM (512 columns): two S slots of B_K columns (P, in
+// 16 bits, overwrites the first B_K / 2 columns of its S slot) and OS fp32 O
+// accumulators of d columns.
 __host__ __device__ constexpr int fwd_qs(int d, int bk) {
-  return d == 64 ? 4 : (d == 128 ? 3 : (bk == 128 ? 1 : 2));
+  return d == 64 ? 4 : (d == 128 ? (bk == 128 ? 2 : 4) : (bk == 128 ? 1 : 2));
 }
 __host__ __device__ constexpr int fwd_kvs(int d, int bk) {
-  return (d == 64 || (d == 128 && bk <= 64)) ? 2 : 1;
+  return d == 256 ? (bk <= 32 ? 2 : 1) : 2;
 }
-__host__ __device__ constexpr int fwd_ps(int d, int bk) { return (d == 256 && bk == 128) ? 1 : 2; }
-__host__ __device__ constexpr int fwd_os(int d) { return d == 256 ? 1 : 2; }
+__host__ __device__ constexpr int fwd_os(int d, int bk) { return 2 * bk + 2 * d <= 512 ? 2 : 1; }
 
 template <int D, int BK>
 struct FwdSmem {
-  static constexpr int QS = fwd_qs(D, BK), KVS = fwd_kvs(D, BK), PS = fwd_ps(D, BK),
-                       OS = fwd_os(D);
-  static constexpr int kPCols = BK < 64 ? 64 : BK;
-  static constexpr uint32_t kQ = 128u * D * 2u;            // one Q stage (and output staging)
+  static constexpr int QS = fwd_qs(D, BK), KVS = fwd_kvs(D, BK), OS = fwd_os(D, BK);
+  static constexpr uint32_t kQ = 128u * D * 2u;            // one Q stage
   static constexpr uint32_t kK = uint32_t(BK) * D * 2u;     // one K (or V) stage
-  static constexpr uint32_t kP = 128u * kPCols * 2u;        // one P buffer
+  static constexpr uint32_t kStg = 128u * 64u * 2u;         // one staging slot
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kOffQ + QS * kQ;
   static constexpr uint32_t kOffV = kOffK + KVS * kK;
-  static constexpr uint32_t kOffP = kOffV + KVS * kK;
-  static constexpr uint32_t kBytes = kOffP + PS * kP + 1024;   // + alignment slack
+  static constexpr uint32_t kOffStg = kOffV + KVS * kK;
+  static constexpr uint32_t kBytes = kOffStg + 2 * kStg + 1024;   // + alignment slack
   static_assert(kBytes <= 227u * 1024u, "shared memory budget");
   static_assert(2 * BK + OS * D <= 512, "TMEM budget");
   static constexpr uint32_t kTmemCols = 512;
 };
 
-constexpr int kFwdThreads = 384;   // warp 0 MMA, warp 2 TMA producer, warps 4-11 two softmax WGs
+// warps 0-3 Q producers, warp 4 MMA, warp 5 TMEM owner, warp 6 K/V producer,
+// warps 8-11 / 12-15 two softmax WGs
+constexpr int kFwdThreads = 512;
+
+// The tiles of one CTA: chunks of `C` consecutive tiles, chunk c going to CTA
+// c % gridDim.x.  C = 0 means one contiguous range per CTA.
+struct TileSeq {
+  int total, C, chunk, in_chunk;
+  __device__ __forceinline__ void init(int total_, int c) {
+    total = total_;
+    C = c > 0 ? c : max(1, (total_ + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x));
+    chunk = blockIdx.x;
+    in_chunk = 0;
+  }
+  __device__ __forceinline__ int tile() const { return chunk * C + in_chunk; }
+  __device__ __forceinline__ bool valid() const { return chunk * C + in_chunk < total; }
+  __device__ __forceinline__ void next() {
+    if (++in_chunk == C || chunk * C + in_chunk >= total) {
+      in_chunk = 0;
+      chunk += gridDim.x;
+    }
+  }
+};
+
+__device__ __forceinline__ TileDesc load_desc(const Params &p, const TileSeq &s) {
+  if (!s.valid()) return TileDesc{0, 0, -1, -1};
+  const int4 v = __ldg(reinterpret_cast<const int4 *>(p.tdesc) + s.tile());
+  return TileDesc{v.x, v.y, v.z, v.w};
+}
 
 // Persistent, warp-specialised forward main kernel (one CTA per SM).
-//   warp 2 (lane 0 + lanes for row coordinates): TMA loads -- K_b and V_b tiles
-//     (3-D tensor maps, once per segment) and the 128 gathered Q rows of each
-//     tile (tile::gather4 of four rows at a time), 128-byte swizzled;
-//   warp 0 (one thread): tcgen05 MMAs S(i) = Q K^T into TMEM slot i % 2 and
+//   warps 0-3: producer -- the gathered Q rows of each tile by cp.async (16-byte
+//     chunks, a warp instruction covering 256 / d whole rows, so reads are fully
+//     coalesced), written into the 128-byte-swizzled operand layout.  A Q stage
+//     is released as soon as the S MMA that reads it completes;
+//   warp 6 (one thread): K_b and V_b by TMA (3-D tensor maps, once per change of
+//     (KV head, block));
+//   warp 4 (one thread): tcgen05 MMAs S(i) = Q K^T into TMEM slot i % 2 and
 //     O(i) = P V into an O accumulator, issued as S(0), S(1), O(0), S(2), O(1), ...;
-//   warps 4-7 / 8-11: softmax of even / odd tiles (row max, exp2, P in 16-bit
-//     to shared memory, fp32 row sum) and their epilogue (O from TMEM to 16-bit,
-//     staged in the tile's Q stage, one bulk store of the tile's contiguous
-//     compact-buffer rows, (m, l) per row).
+//   warps 8-11 / 12-15: softmax of even / odd tiles (row max, exp2, P in 16 bits
+//     back to TMEM, fp32 row sum) and their epilogue (O from TMEM to 16 bits,
+//     staged one 64-column block at a time and written by TMA tensor stores to
+//     the tile's 128 rows of the compact buffer; (m, l) per row).
 // mbarriers hand each buffer between roles; every wait is bounded.
 template <int D, int BK, bool kFp16>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, Params p) {
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_o, Params p) {
   using L = FwdSmem<D, BK>;
-  constexpr int QS = L::QS, KVS = L::KVS, PS = L::PS, OS = L::OS;
+  constexpr int QS = L::QS, KVS = L::KVS, OS = L::OS;
   constexpr int kCB = D / 64;                      // 64-column blocks per row
   constexpr uint32_t kIdescS = idesc_f16(128, BK, false, false, kFp16);
   constexpr uint32_t kIdescO = idesc_f16(128, D, false, true, kFp16);
 
   extern __shared__ uint8_t smem_raw[];
-  // Barriers a softmax warpgroup waits on (s_full, p_empty, o_full) are per warpgroup
-  // (index i & 1) whatever the buffer counts, so no waiter is ever two phases ahead.
   __shared__ uint64_t q_full[QS], q_empty[QS], kv_full[KVS], kv_empty[KVS], s_full[2],
-      p_full[PS], p_empty[2], o_full[2], o_free[OS];
+      p_full[2], o_full[2], o_free[OS];
+  // Per Q stage: K/V flags of the stage's tile, written by the producer before it
+  // arms q_full and read by the MMA thread after q_full completes:
+  //   bits 0-7 K/V stage, bit 8 first tile of that K/V, bit 9 last tile of it.
+  __shared__ uint32_t q_flags[QS];
   __shared__ uint32_t tmem_base;
   __shared__ int fail;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   const uint32_t sQ0 = smem_u32(smem + L::kOffQ), sK0 = smem_u32(smem + L::kOffK),
-                 sV0 = smem_u32(smem + L::kOffV), sP0 = smem_u32(smem + L::kOffP);
+                 sV0 = smem_u32(smem + L::kOffV), sStg0 = smem_u32(smem + L::kOffStg);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  if (warp == 0) tmem_alloc(&tmem_base, L::kTmemCols);
-  if (tid == 32) {
-    for (int i = 0; i < QS; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
+  if (warp == 5) tmem_alloc(&tmem_base, L::kTmemCols);
+  if (tid == 0) {
+    for (int i = 0; i < QS; ++i) { mbar_init(&q_full[i], 128); mbar_init(&q_empty[i], 1); }
     for (int i = 0; i < KVS; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_empty[i], 1);
+      mbar_init(&p_full[i], 128);
       mbar_init(&o_full[i], 1);
     }
-    for (int i = 0; i < PS; ++i) mbar_init(&p_full[i], 128);
     for (int i = 0; i < OS; ++i) mbar_init(&o_free[i], 128);
     fail = 0;
     fence_mbar_init();
@@ -111,113 +145,183 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tS0 = tmem_base, tO0 = tmem_base + 2 * BK;
+  const int total = p.wtile_off[p.nsub];
 
-  const int nb = *p.nb;
-  const int nseg = p.h_k * nb;
-  const int total_tiles = p.tile_off[nseg];
-  const int per_cta = (total_tiles + gridDim.x - 1) / gridDim.x;
-  const int t_begin = min(total_tiles, static_cast<int>(blockIdx.x) * per_cta);
-  const int n = min(total_tiles, t_begin + per_cta) - t_begin;
-
-  if (warp == 2) {
+  if (warp < 4) {
     // ------------------------------ producer ------------------------------
-    if (n > 0) {
-      TileCursor cur;
-      cur.start(p, nb, t_begin);
-      const int oob_row = p.n * p.h_q;     // zero-filled by the tensor map
-      for (int i = 0; i < n; ++i) {
-        cur.set(p, t_begin + i);
-        if (cur.new_seg) {
-          const int ks = cur.jseg % KVS;
-          if (cur.jseg >= KVS) mbar_wait_sticky(&kv_empty[ks], ((cur.jseg / KVS) - 1) & 1, p.status, &fail);
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&kv_full[ks], 2u * L::kK);
+    constexpr int kCPR = D / 8;           // 16-byte chunks per row
+    constexpr int kRPI = 32 / kCPR;       // rows per warp instruction
+    constexpr int kLag = QS - 1;          // tiles whose copies stay in flight
+    const int pt = tid, pw = pt >> 5;
+    TileSeq seq;
+    seq.init(total, p.fwd_chunk);
+    const int oob_row = p.n * p.h_q;
+    // global Q row of tile row 32 pw + lane (oob_row for padding rows)
+    auto row_id = [&](const TileDesc &d) {
+      const int h = d.hn & 0xffff, nrows = d.hn >> 16, r = pw * 32 + lane;
+      if (r >= nrows) return oob_row;
+      const int rr = d.row0 + r;
+      const int t = __ldg(p.q_list + d.q_off + rr / p.g);
+      return t * p.h_q + h * p.g + rr % p.g;
+    };
+    const uint16_t *gq = static_cast<const uint16_t *>(p.q);
+    int li = 0, kv_n = 0, prev_h = -1, prev_key0 = -1;
+    TileDesc dc = load_desc(p, seq);
+    TileSeq seq1 = seq;
+    seq1.next();
+    TileDesc dn = load_desc(p, seq1);
+    int rid_c = seq.valid() ? row_id(dc) : oob_row;
+    while (seq.valid()) {
+      TileSeq seq2 = seq1;
+      seq2.next();
+      const TileDesc dnn = load_desc(p, seq2);               // two tiles ahead
+      const int rid_n = seq1.valid() ? row_id(dn) : oob_row;  // one tile ahead
+      // K/V flags of this tile for the MMA thread (the loads are warp 6's)
+      const int h = dc.hn & 0xffff;
+      const bool first = h != prev_h || dc.key0 != prev_key0;
+      const bool last = !seq1.valid() || (dn.hn & 0xffff) != h || dn.key0 != dc.key0;
+      if (first) {
+        ++kv_n;
+        prev_h = h;
+        prev_key0 = dc.key0;
+      }
+      const int qs = li % QS;
+      if (li >= QS) mbar_wait_sticky(&q_empty[qs], ((li / QS) - 1) & 1, p.status, &fail);
+      if (pt == 0)
+        q_flags[qs] = static_cast<uint32_t>((kv_n - 1) % KVS) | (first ? 0x100u : 0u) |
+                      (last ? 0x200u : 0u);
+      const uint32_t stage = sQ0 + qs * L::kQ;
 #pragma unroll
-            for (int cb = 0; cb < kCB; ++cb) {
-              tma_load_3d(sK0 + ks * L::kK + cb * BK * 128, &tm_k, cb * 64, cur.h, cur.key0, &kv_full[ks]);
-              tma_load_3d(sV0 + ks * L::kK + cb * BK * 128, &tm_v, cb * 64, cur.h, cur.key0, &kv_full[ks]);
-            }
+      for (int ins = 0; ins < kCPR; ++ins) {
+        const int src_lane = ins * kRPI + lane / kCPR;
+        const int rid = __shfl_sync(0xffffffffu, rid_c, src_lane);
+        const int chunk = lane % kCPR;
+        const bool in = rid < oob_row;
+        cp_async16(stage + sw128_offset(pw * 32 + src_lane, chunk, 128),
+                   gq + (in ? (int64_t)rid * D + chunk * 8 : 0), in ? 16u : 0u);
+      }
+      cp_async_commit();
+      if (li >= kLag) {
+        cp_async_wait_group<kLag>();
+        fence_proxy_async_smem();
+        mbar_arrive(&q_full[(li - kLag) % QS]);
+      }
+      ++li;
+      seq = seq1;
+      seq1 = seq2;
+      dc = dn;
+      dn = dnn;
+      rid_c = rid_n;
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    for (int j = li - kLag > 0 ? li - kLag : 0; j < li; ++j) mbar_arrive(&q_full[j % QS]);
+  } else if (warp == 6) {
+    // --------------------------- K/V producer -----------------------------
+    // A warp of its own: its waits on kv_empty must not hold back the Q
+    // producers, whose q_full arrivals lag their copies by QS - 1 tiles.
+    if (lane == 0) {
+      TileSeq seq;
+      seq.init(total, p.fwd_chunk);
+      int kv_n = 0, prev_h = -1, prev_key0 = -1;
+      TileDesc dc = load_desc(p, seq);
+      TileSeq seq1 = seq;
+      seq1.next();
+      TileDesc dn = load_desc(p, seq1);
+      while (seq.valid()) {
+        TileSeq seq2 = seq1;
+        seq2.next();
+        const TileDesc dnn = load_desc(p, seq2);
+        const int h = dc.hn & 0xffff;
+        if (h != prev_h || dc.key0 != prev_key0) {
+          const int ks = kv_n % KVS;
+          if (kv_n >= KVS)
+            mbar_wait_sticky(&kv_empty[ks], ((kv_n / KVS) - 1) & 1, p.status, &fail);
+          mbar_arrive_expect_tx(&kv_full[ks], 2u * L::kK);
+#pragma unroll
+          for (int cb = 0; cb < kCB; ++cb) {
+            tma_load_3d(sK0 + ks * L::kK + cb * BK * 128, &tm_k, cb * 64, h, dc.key0, &kv_full[ks]);
+            tma_load_3d(sV0 + ks * L::kK + cb * BK * 128, &tm_v, cb * 64, h, dc.key0, &kv_full[ks]);
           }
+          ++kv_n;
+          prev_h = h;
+          prev_key0 = dc.key0;
         }
-        const int qs = i % QS;
-        if (i >= QS) mbar_wait_sticky(&q_empty[qs], ((i / QS) - 1) & 1, p.status, &fail);
-        if (lane == 0) mbar_arrive_expect_tx(&q_full[qs], L::kQ);
-        __syncwarp();
-        int rows[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = lane * 4 + j;
-          if (r < cur.nrows) {
-            const int rr = cur.row0 + r;
-            const int t = p.q_list[cur.seg_off + rr / p.g];
-            rows[j] = t * p.h_q + cur.h * p.g + rr % p.g;
-          } else {
-            rows[j] = oob_row;
-          }
-        }
-#pragma unroll
-        for (int cb = 0; cb < kCB; ++cb)
-          tma_gather4(sQ0 + qs * L::kQ + cb * 128 * 128 + lane * 4 * 128, &tm_q, cb * 64, rows[0],
-                      rows[1], rows[2], rows[3], &q_full[qs]);
+        seq = seq1;
+        seq1 = seq2;
+        dc = dn;
+        dn = dnn;
       }
     }
-  } else if (warp == 0) {
+  } else if (warp == 4) {
     // ------------------------------ MMA issuer ------------------------------
-    if (lane == 0 && n > 0) {
-      TileCursor cs, co;   // S stream runs two tiles ahead of the O stream
-      cs.start(p, nb, t_begin);
-      co.start(p, nb, t_begin);
-      auto issue_s = [&](int i) {
-        cs.set(p, t_begin + i);
-        const int ks = cs.jseg % KVS, qs = i % QS;
-        if (cs.new_seg) mbar_wait_sticky(&kv_full[ks], (cs.jseg / KVS) & 1, p.status, &fail);
+    if (lane == 0) {
+      TileSeq seq;
+      seq.init(total, p.fwd_chunk);
+      int n = 0;    // tiles of this CTA
+      for (TileSeq c = seq; c.valid(); c.next()) ++n;
+      uint32_t flags[2] = {0u, 0u};   // K/V flags of tiles i and i + 1 (index i & 1)
+      int s_next = 0;                 // next tile whose S has to be issued
+      int s_kv = 0;                   // K/V loads consumed so far (load m fills stage m % KVS)
+      auto issue_s = [&]() {
+        const int i = s_next, qs = i % QS;
         mbar_wait_sticky(&q_full[qs], (i / QS) & 1, p.status, &fail);
+        const uint32_t f = q_flags[qs];
+        flags[i & 1] = f;
+        const int ks = static_cast<int>(f & 0xffu);
+        if (f & 0x100u) {
+          // load s_kv is the (s_kv / KVS)-th fill of stage s_kv % KVS (== ks)
+          mbar_wait_sticky(&kv_full[ks], (s_kv / KVS) & 1, p.status, &fail);
+          ++s_kv;
+        }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_f16(tS0 + (i & 1) * BK, desc_kmajor(sQ0 + qs * L::kQ, 128, kk),
                   desc_kmajor(sK0 + ks * L::kK, BK, kk), kIdescS, kk > 0);
         mma_commit(&s_full[i & 1]);
+        mma_commit(&q_empty[qs]);
+        ++s_next;
       };
-      // S(i + 1) is issued ahead of O(i) unless its Q stage or K/V buffer is only
-      // released by O(i) itself (single-buffered configurations).
-      int next_s = 0;
       for (int i = 0; i < n; ++i) {
-        if (next_s == i) issue_s(next_s++);
-        if (next_s == i + 1 && i + 1 < n && QS >= 2 &&
-            !(KVS == 1 && t_begin + i + 1 >= cs.seg_end_tile))
-          issue_s(next_s++);
-        co.set(p, t_begin + i);
-        const int ks = co.jseg % KVS, ps = i % PS, os = i % OS;
-        mbar_wait_sticky(&p_full[ps], (i / PS) & 1, p.status, &fail);
+        if (s_next == i) issue_s();
+        // S(i + 1) goes ahead of O(i) unless its K/V stage is only released by O(i)
+        // itself (a single K/V stage and a change of block after tile i).
+        if (s_next == i + 1 && i + 1 < n && !(KVS == 1 && (flags[i & 1] & 0x200u))) issue_s();
+        const uint32_t f = flags[i & 1];
+        const int ks = static_cast<int>(f & 0xffu), os = i % OS;
+        mbar_wait_sticky(&p_full[i & 1], (i >> 1) & 1, p.status, &fail);
         if (i >= OS) mbar_wait_sticky(&o_free[os], ((i / OS) - 1) & 1, p.status, &fail);
         tc_fence_after();
+        const uint32_t tP = tS0 + (i & 1) * BK;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          mma_f16(tO0 + os * D, desc_kmajor(sP0 + ps * L::kP, 128, kk),
-                  desc_mnmajor(sV0 + ks * L::kK, BK, kk), kIdescO, kk > 0);
+          mma_f16_ts(tO0 + os * D, tP + kk * 8, desc_mnmajor(sV0 + ks * L::kK, BK, kk), kIdescO,
+                     kk > 0);
         mma_commit(&o_full[i & 1]);
-        mma_commit(&p_empty[i & 1]);
-        if (t_begin + i + 1 == co.seg_end_tile || i + 1 == n) mma_commit(&kv_empty[ks]);
+        if (f & 0x200u) mma_commit(&kv_empty[ks]);
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 8) {
     // ------------------------- softmax + epilogue -------------------------
-    const int wg = (warp - 4) >> 2;
-    const int row = tid - 128 - wg * 128;                  // tile row = TMEM lane
+    const int wg = (warp - 8) >> 2;
+    const int row = tid - 256 - wg * 128;                  // tile row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    TileCursor cur;
-    if (n > 0) cur.start(p, nb, t_begin);
-    uint16_t *obuf = static_cast<uint16_t *>(p.obuf);
-    for (int i = wg; i < n; i += 2) {
-      cur.set(p, t_begin + i);
-      const bool row_in = row < cur.nrows;
+    const uint32_t stg = sStg0 + wg * L::kStg;
+    TileSeq seq;
+    seq.init(total, p.fwd_chunk);
+    if (wg == 1) seq.next();
+    for (int i = wg; seq.valid(); i += 2) {
+      const int tile = seq.tile();
+      const TileDesc dsc = load_desc(p, seq);
+      const int nrows = dsc.hn >> 16;
+      const bool row_in = row < nrows;
       int lim = -1;
       if (row_in) {
-        const int t = p.q_list[cur.seg_off + (cur.row0 + row) / p.g];
-        lim = min(BK - 1, t - cur.key0);
+        const int t = __ldg(p.q_list + dsc.q_off + (dsc.row0 + row) / p.g);
+        lim = min(BK - 1, t - dsc.key0);
       }
-      const int ps = i % PS, os = i % OS, qs = i % QS;
+      const int os = i % OS;
       mbar_wait_sticky(&s_full[i & 1], (i >> 1) & 1, p.status, &fail);
       tc_fence_after();
       const uint32_t tS = tS0 + (i & 1) * BK + lane_off;
@@ -231,12 +335,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (c * 32 + j <= lim) mx = fmaxf(mx, sv[j]);
       }
       const float m2 = row_in ? mx * p.scale_log2 : 0.f;
-      // the P buffer is free once O of the previous tile that used it is done
-      if (PS == 2 && i >= 2) mbar_wait_sticky(&p_empty[i & 1], ((i >> 1) - 1) & 1, p.status, &fail);
-      if (PS == 1 && i >= 1)
-        mbar_wait_sticky(&p_empty[(i - 1) & 1], ((i - 1) >> 1) & 1, p.status, &fail);
       float lsum = 0.f;
-      const uint32_t sP = sP0 + ps * L::kP;
 #pragma unroll
       for (int c = 0; c < BK / 32; ++c) {
         float sv[32];
@@ -250,61 +349,59 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           lsum += p0 + p1;                    // fp32 row sum (exact lse)
           pk[j / 2] = pack2<kFp16>(p0, p1);   // P rounded to 16 bits for the PV MMA
         }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint32_t so = sw128_offset(row, c * 4 + q4, 128);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sP + so), "r"(pk[q4 * 4]),
-                       "r"(pk[q4 * 4 + 1]), "r"(pk[q4 * 4 + 2]), "r"(pk[q4 * 4 + 3])
-                       : "memory");
-        }
+        // 32 P values of this chunk -> 16 TMEM columns; they overwrite S columns
+        // [16 c, 16 c + 16), which this thread has already read.
+        tmem_st16(tS + c * 16, pk);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[ps]);
+      mbar_arrive(&p_full[i & 1]);
 
-      // epilogue: O(i) -> 16-bit, staged (swizzled) in this tile's Q stage, then
-      // copied to the tile's contiguous compact-buffer rows with coalesced stores
+      // epilogue: O(i) -> 16-bit, one 64-column block at a time through this
+      // warpgroup's staging slot, TMA-stored to the tile's 128 compact-buffer rows
       mbar_wait_sticky(&o_full[i & 1], (i >> 1) & 1, p.status, &fail);
       tc_fence_after();
-      const uint32_t stage = sQ0 + qs * L::kQ;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float ov[32];
-        tmem_ld32(tO0 + os * D + c * 32 + lane_off, ov);
-        uint32_t pk[16];
+      for (int cb = 0; cb < kCB; ++cb) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) pk[j / 2] = pack2<kFp16>(ov[j], ov[j + 1]);
+        for (int half = 0; half < 2; ++half) {
+          float ov[32];
+          tmem_ld32(tO0 + os * D + cb * 64 + half * 32 + lane_off, ov);
+          uint32_t pk[16];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint32_t so = sw128_offset(row, c * 4 + q4, 128);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + so),
-                       "r"(pk[q4 * 4]), "r"(pk[q4 * 4 + 1]), "r"(pk[q4 * 4 + 2]),
-                       "r"(pk[q4 * 4 + 3])
-                       : "memory");
+          for (int j = 0; j < 32; j += 2) pk[j / 2] = pack2<kFp16>(ov[j], ov[j + 1]);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint32_t so = sw128_offset(row, half * 4 + q4, 128);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg + so),
+                         "r"(pk[q4 * 4]), "r"(pk[q4 * 4 + 1]), "r"(pk[q4 * 4 + 2]),
+                         "r"(pk[q4 * 4 + 3])
+                         : "memory");
+          }
         }
+        if (cb == kCB - 1) {
+          tc_fence_before();
+          mbar_arrive(&o_free[os]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1 + wg, 128);
+        if (row == 0) {
+          tma_store_2d(&tm_o, stg, cb * 64, tile * kTileRows);
+          bulk_commit();
+          bulk_wait_read_all();   // the slot is rewritten by the next column block
+        }
+        named_bar_sync(1 + wg, 128);
       }
-      tc_fence_before();
-      mbar_arrive(&o_free[os]);
-      const int64_t grow0 = (int64_t)cur.seg_off * p.g + cur.row0;
-      if (row_in) p.mlbuf[grow0 + row] = make_float2(m2, lsum);
-      named_bar_sync(1 + wg, 128);
-      constexpr int kRowChunks = D / 8;
-      for (int idx = row; idx < cur.nrows * kRowChunks; idx += 128) {
-        const int r = idx / kRowChunks, ch = idx - r * kRowChunks;
-        uint4 val;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                     : "r"(stage + sw128_offset(r, ch, 128)));
-        *reinterpret_cast<uint4 *>(obuf + (grow0 + r) * D + ch * 8) = val;
-      }
-      named_bar_sync(1 + wg, 128);
-      if (row == 0) mbar_arrive(&q_empty[qs]);
+      p.mlbuf[(int64_t)tile * kTileRows + row] = make_float2(m2, lsum);
+      seq.next();
+      seq.next();
     }
+    if (row == 0) bulk_wait_all();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem_base, L::kTmemCols);
+  if (warp == 5) tmem_dealloc(tmem_base, L::kTmemCols);
 }
 
 // One warp per (token, query head): combine the <= T partials.
@@ -318,8 +415,8 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(Params p) {
   const int h = hq / p.g, j = hq - h * p.g;
   int64_t row = -1;
   if (lane < p.topk) {
-    const int32_t pos = p.slot_map[((int64_t)h * p.n + t) * p.topk + lane];
-    if (pos >= 0) row = (int64_t)pos * p.g + j;
+    const int32_t pr = p.prow[((int64_t)h * p.n + t) * p.topk + lane];
+    if (pr >= 0) row = (int64_t)pr + j;
   }
   float2 ml = make_float2(-INFINITY, 0.f);
   if (row >= 0) ml = p.mlbuf[row];
@@ -414,12 +511,23 @@ bool make_qkv_maps(const Params &p, const void *q, CUtensorMap *mq, CUtensorMap 
          encode_map(mv, f16, 3, p.v, kdims, kstr, kbox);
 }
 
+// Tensor map of the compact partial buffer: [max_tiles * 128 rows, d], box =
+// 128 rows x 64 columns, 128-byte swizzle (the staging slot's layout).
+static bool make_obuf_map(const Params &p, int64_t max_tiles, CUtensorMap *mo) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.d),
+                              static_cast<cuuint64_t>(max_tiles) * kTileRows};
+  const cuuint64_t str[1] = {static_cast<cuuint64_t>(p.d) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTileRows)};
+  return encode_map(mo, p.dtype == NSA_FP16, 2, p.obuf, dims, str, box);
+}
+
 template <int D, int BK, bool kFp16>
 static cudaError_t run_fwd(const Params &p, int num_sms, int64_t max_tiles, cudaStream_t stream,
                            void (*mark)(int, cudaStream_t, bool)) {
   using L = FwdSmem<D, BK>;
-  CUtensorMap mq, mk, mv;
-  if (!make_qkv_maps(p, p.q, &mq, &mk, &mv)) return cudaErrorInvalidValue;
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_qkv_maps(p, p.q, &mq, &mk, &mv) || !make_obuf_map(p, max_tiles, &mo))
+    return cudaErrorInvalidValue;
   // One CTA per SM: it owns all 512 TMEM columns.
   const uint32_t smem = L::kBytes > 120u * 1024u ? L::kBytes : 120u * 1024u;
   cudaError_t e = cudaFuncSetAttribute(fwd_main_kernel<D, BK, kFp16>,
@@ -430,7 +538,7 @@ static cudaError_t run_fwd(const Params &p, int num_sms, int64_t max_tiles, cuda
   if (grid > max_tiles) grid = max_tiles > 0 ? max_tiles : 1;
   mark(5, stream, true);
   fwd_main_kernel<D, BK, kFp16>
-      <<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, p);
+      <<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, mo, p);
   mark(5, stream, false);
   const int64_t rows = static_cast<int64_t>(p.n) * p.h_q;
   mark(6, stream, true);

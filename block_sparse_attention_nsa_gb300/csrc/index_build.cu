@@ -3,13 +3,19 @@
 // tensors of "FSA: An Alternative Efficient Implementation of Native Sparse
 // Attention Kernel", key design 2.  It is a stable counting sort of the kept
 // (token, slot) pairs by (KV head, global block):
-//   geometry  -> per-sequence first global block, NB
-//   count     -> per token-tile histogram over blocks (tile = kIdxWarps x 32 tokens)
-//   col_scan  -> per block, exclusive prefix over token tiles, block totals
-//   scan      -> exclusive prefix over (head, block): offsets, tile and chunk offsets
-//   scatter   -> positions: block offset + earlier tiles + earlier warps + rank in warp
+//   geometry   -> per-sequence first global block, NB
+//   count      -> per token-tile histogram over blocks, kept pairs per token
+//   col_scan   -> per block, exclusive prefix over token tiles, block totals
+//   scan       -> exclusive prefix over (head, block): offsets, tile and chunk offsets
+//   wave_scan  -> forward tiles of every (head, wave, block) sub-segment, prefix
+//   tile_desc  -> one descriptor per forward tile
+//   scatter    -> positions: block offset + earlier tiles + rank inside the tile
 // Tokens inside a block's list come out ascending and duplicates keep their first
-// slot, so the result is unique and bit-reproducible (no atomics decide order).
+// slot, so the result is unique and bit-reproducible: ranks come from per-block
+// token bitmasks (population counts), not from the order of atomic operations.
+//
+// One thread handles one token: it reads the token's T slots, drops invalid and
+// repeated values in registers, and names each kept block once.
 #include "common.cuh"
 
 namespace nsa {
@@ -72,76 +78,62 @@ __global__ void __launch_bounds__(1024) geometry_kernel(Params p) {
 }
 
 // ---------------------------------------------------------------------------
-// One pass over a warp's 32 tokens, in token order.  Lanes cover (token, slot)
-// pairs: tokens_per_step = 32 / TP tokens per step, TP = next power of two >= T.
-// kScatter = false: counts per block into bins (this warp's shared-memory row).
-// kScatter = true : bins hold this warp's running base position per block; writes
-//                   q_list and slot_map.
+// The kept blocks of token t for KV head h: kgb[k] = global block of slot k, or
+// -1 when slot k is empty, out of range, in the future, or repeats an earlier
+// slot.  Returns the number of kept slots; raises *bad for values below -1 or
+// past the sequence's last block.  TP = T rounded up to a power of two.
 // ---------------------------------------------------------------------------
-template <bool kScatter>
-__device__ __forceinline__ void walk_tokens(const Params &p, int h, int tok0, int tok_end,
-                                            int tp, int32_t *bins, int nb) {
-  const int lane = threadIdx.x & 31;
-  const int tps = 32 / tp;
-  const int slot = lane & (tp - 1), sub = lane / tp;
-  for (int base = tok0; base < tok_end; base += tps) {
-    const int t = base + sub;
-    const bool live = (slot < p.topk) && (t < tok_end);
-    int32_t b = -1;
-    int gb = -1;
-    bool ok = false;
-    if (live) {
-      b = __ldg(p.sel + ((int64_t)h * p.n + t) * p.topk + slot);
-      const int s = seq_of(p.cu, p.num_seqs, t);
-      const int tau = t - p.cu[s];
-      const int nblk = p.blk_start[s + 1] - p.blk_start[s];
-      ok = (b >= 0) && (b <= tau / p.block) && (b < nblk);
-      if (!kScatter && (b < -1 || b >= nblk)) set_status(p.status, NSA_DEVERR_BAD_INDEX);
-      gb = p.blk_start[s] + b;
-    }
-    // duplicates inside one token: the lowest slot keeps the block
-    const uint64_t key1 = ok ? ((static_cast<uint64_t>(sub) << 32) | static_cast<uint32_t>(b))
-                             : (0xFFFFFFFF00000000ull | static_cast<uint64_t>(lane));
-    const uint32_t m1 = __match_any_sync(0xffffffffu, key1);
-    const bool keep = ok && ((__ffs(m1) - 1) == lane);
-    // lanes of different tokens naming the same block (at most one lane per token)
-    const uint32_t key2 = keep ? static_cast<uint32_t>(gb) : (0x80000000u | lane);
-    const uint32_t m2 = __match_any_sync(0xffffffffu, key2);
-    const bool leader = keep && ((__ffs(m2) - 1) == lane);
-    if constexpr (!kScatter) {
-      if (leader) bins[gb] += __popc(m2);
-    } else {
-      int32_t pos = -1;
-      if (keep) pos = bins[gb] + __popc(m2 & ((1u << lane) - 1u));
-      __syncwarp();
-      if (leader) bins[gb] += __popc(m2);
-      __syncwarp();
-      if (live) {
-        p.slot_map[((int64_t)h * p.n + t) * p.topk + slot] = pos;
-        if (keep) p.q_list[pos] = t;
-      }
-    }
+template <int TP>
+__device__ __forceinline__ int token_blocks(const Params &p, int nb, int h, int t,
+                                            int32_t (&kgb)[TP], bool &bad) {
+  const int s = seq_of(p.cu, p.num_seqs, t);
+  const int tau = t - __ldg(p.cu + s);
+  const int c = tau / p.block;
+  const int bs = p.blk_start[s];
+  const int nblk = p.blk_start[s + 1] - bs;
+  const int32_t *row = p.sel + ((int64_t)h * p.n + t) * p.topk;
+  int np = 0;
+#pragma unroll
+  for (int k = 0; k < TP; ++k) {
+    const bool in = k < p.topk;
+    const int b = in ? __ldg(row + k) : -1;
+    if (in && (b < -1 || b >= nblk)) bad = true;
+    bool ok = in && b >= 0 && b <= c && b < nblk && bs + b < nb;
+#pragma unroll
+    for (int j = 0; j < k; ++j) ok = ok && (kgb[j] != bs + b);
+    kgb[k] = ok ? bs + b : -1;
+    np += ok ? 1 : 0;
   }
-  (void)nb;
+  return np;
 }
 
-// grid (n_idx_tiles, h_k), block idx_warps*32; dynamic smem idx_warps * nb_max ints
-__global__ void __launch_bounds__(kIdxWarps * 32) count_kernel(Params p, int tp) {
-  extern __shared__ int32_t bins_all[];
+// grid (n_idx_tiles, h_k), block kIdxThreads; dynamic smem nb_max ints.
+// chunk_hist[h][tile][gb] = kept pairs of the tile's tokens naming block gb;
+// npairs[h][t] = kept pairs of token t.
+template <int TP>
+__global__ void __launch_bounds__(kIdxThreads) count_kernel(Params p) {
+  extern __shared__ int32_t bins[];
   const int nb = *p.nb;
-  const int h = blockIdx.y, tile = blockIdx.x, W = p.idx_warps;
-  const int warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < W * nb; i += blockDim.x) bins_all[i] = 0;
+  const int h = blockIdx.y, tile = blockIdx.x, tid = threadIdx.x;
+  for (int i = tid; i < nb; i += blockDim.x) bins[i] = 0;
   __syncthreads();
-  const int tok0 = (tile * W + warp) * 32;
-  if (tok0 < p.n) walk_tokens<false>(p, h, tok0, min(p.n, tok0 + 32), tp, bins_all + warp * nb, nb);
+  const int t = tile * p.idx_tok + tid;
+  if (tid < p.idx_tok && t < p.n) {
+    int32_t kgb[TP];
+    bool bad = false;
+    int np = 0;
+    if (nb > 0) {
+      np = token_blocks<TP>(p, nb, h, t, kgb, bad);
+#pragma unroll
+      for (int k = 0; k < TP; ++k)
+        if (kgb[k] >= 0) atomicAdd(&bins[kgb[k]], 1);
+    }
+    if (bad) set_status(p.status, NSA_DEVERR_BAD_INDEX);
+    p.npairs[(int64_t)h * p.n + t] = np;
+  }
   __syncthreads();
   int32_t *hist = p.chunk_hist + ((int64_t)h * p.n_idx_tiles + tile) * p.nb_max;
-  for (int gb = threadIdx.x; gb < nb; gb += blockDim.x) {
-    int32_t s = 0;
-    for (int w = 0; w < W; ++w) s += bins_all[w * nb + gb];
-    hist[gb] = s;
-  }
+  for (int gb = tid; gb < nb; gb += blockDim.x) hist[gb] = bins[gb];
 }
 
 // grid (ceil(nb_max / 32), h_k), block (32, 8): exclusive prefix over token tiles
@@ -228,45 +220,212 @@ __global__ void __launch_bounds__(1024) scan_kernel(Params p) {
   }
 }
 
-// Same grid as count_kernel.
-__global__ void __launch_bounds__(kIdxWarps * 32) scatter_kernel(Params p, int tp) {
-  extern __shared__ int32_t bins_all[];
+// ---------------------------------------------------------------------------
+// Forward sub-segments.  Wave w covers index token tiles [w * wave_tiles,
+// (w + 1) * wave_tiles); the tokens of wave w that selected block gb are a
+// contiguous run of the block's ascending list I_gb, starting at the exclusive
+// prefix chunk_hist[h][w * wave_tiles][gb].  Sub-segment id:
+// (h * n_w + w) * nb_max + gb.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int32_t wave_lo(const Params &p, int nb, int h, int w, int gb) {
+  const int64_t tile = (int64_t)w * p.wave_tiles;
+  if (tile >= p.n_idx_tiles) return p.counts[h * nb + gb];
+  return p.chunk_hist[((int64_t)h * p.n_idx_tiles + tile) * p.nb_max + gb];
+}
+
+__device__ __forceinline__ void sub_decode(const Params &p, int64_t i, int &h, int &w, int &gb) {
+  gb = static_cast<int>(i % p.nb_max);
+  const int64_t hw = i / p.nb_max;
+  w = static_cast<int>(hw % p.n_w);
+  h = static_cast<int>(hw / p.n_w);
+}
+
+// Rows of sub-segment i and its first list index (lo); 0 rows for blocks >= nb.
+__device__ __forceinline__ int64_t sub_rows(const Params &p, int nb, int64_t i, int32_t *lo_out) {
+  int h, w, gb;
+  sub_decode(p, i, h, w, gb);
+  if (gb >= nb) {
+    *lo_out = 0;
+    return 0;
+  }
+  const int32_t lo = wave_lo(p, nb, h, w, gb), hi = wave_lo(p, nb, h, w + 1, gb);
+  *lo_out = lo;
+  return (int64_t)(hi - lo) * p.g;
+}
+
+// Multi-CTA exclusive scan of the forward tiles per sub-segment: each CTA of
+// 1024 threads scans kScanPer entries locally and records its total.
+__global__ void __launch_bounds__(1024) wave_scan_local_kernel(Params p) {
+  __shared__ int32_t sums[32];
+  constexpr int kPer = kScanPer / 1024;
   const int nb = *p.nb;
-  const int h = blockIdx.y, tile = blockIdx.x, W = p.idx_warps;
-  const int warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < W * nb; i += blockDim.x) bins_all[i] = 0;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t base = (int64_t)blockIdx.x * kScanPer + (int64_t)tid * kPer;
+  int32_t v[kPer];
+  int32_t local = 0;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const int64_t i = base + e;
+    int32_t lo;
+    const int64_t rows = i < p.nsub ? sub_rows(p, nb, i, &lo) : 0;
+    v[e] = static_cast<int32_t>((rows + kTileRows - 1) / kTileRows);
+    local += v[e];
+  }
+  int32_t x = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sums[warp] = x;
   __syncthreads();
-  const int tok0 = (tile * W + warp) * 32;
-  const int tok1 = min(p.n, tok0 + 32);
-  // status bits were raised by the count pass; only the per-warp counts are needed here
-  if (tok0 < p.n) walk_tokens<false>(p, h, tok0, tok1, tp, bins_all + warp * nb, nb);
-  __syncthreads();
-  const int32_t *hist = p.chunk_hist + ((int64_t)h * p.n_idx_tiles + tile) * p.nb_max;
-  for (int gb = threadIdx.x; gb < nb; gb += blockDim.x) {
-    int32_t run = p.offsets[h * nb + gb] + hist[gb];
-    for (int w = 0; w < W; ++w) {
-      const int32_t c = bins_all[w * nb + gb];
-      bins_all[w * nb + gb] = run;
-      run += c;
+  if (warp == 0) {
+    int32_t w = sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
     }
+    sums[lane] = w;
   }
   __syncthreads();
-  if (tok0 < p.n) walk_tokens<true>(p, h, tok0, tok1, tp, bins_all + warp * nb, nb);
+  int32_t run = x - local + (warp > 0 ? sums[warp - 1] : 0);
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const int64_t i = base + e;
+    if (i < p.nsub) p.wtile_off[i] = run;
+    run += v[e];
+  }
+  if (tid == 1023) p.wscan_part[blockIdx.x] = sums[31];
+}
+
+// Adds the totals of earlier CTAs; the last CTA also writes the grand total.
+__global__ void __launch_bounds__(1024) wave_scan_add_kernel(Params p) {
+  __shared__ int32_t base_s;
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    int32_t s = 0;
+    for (int64_t c = tid; c < blockIdx.x; c += 32) s += p.wscan_part[c];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (tid == 0) base_s = s;
+  }
+  __syncthreads();
+  const int32_t b = base_s;
+  const int64_t i0 = (int64_t)blockIdx.x * kScanPer;
+  for (int e = tid; e < kScanPer; e += 1024) {
+    const int64_t i = i0 + e;
+    if (i < p.nsub) p.wtile_off[i] += b;
+  }
+  if (blockIdx.x == gridDim.x - 1 && tid == 0)
+    p.wtile_off[p.nsub] = b + p.wscan_part[blockIdx.x];
+}
+
+// One thread per sub-segment: writes the descriptors of its tiles.
+__global__ void __launch_bounds__(256) tile_desc_kernel(Params p) {
+  const int nb = *p.nb;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= p.nsub) return;
+  const int32_t t0 = p.wtile_off[i], nt = p.wtile_off[i + 1] - t0;
+  if (nt <= 0) return;
+  int h, w, gb;
+  sub_decode(p, i, h, w, gb);
+  int32_t lo;
+  const int64_t rows = sub_rows(p, nb, i, &lo);
+  const int s = upper_index(p.blk_start, p.num_seqs + 1, gb);
+  const int32_t key0 = p.cu[s] + (gb - p.blk_start[s]) * p.block;
+  const int32_t q_off = p.offsets[h * nb + gb] + lo;
+  for (int j = 0; j < nt; ++j) {
+    const int64_t left = rows - (int64_t)j * kTileRows;
+    const int32_t nr = static_cast<int32_t>(left < kTileRows ? left : kTileRows);
+    p.tdesc[t0 + j] = TileDesc{q_off, j * kTileRows, key0, h | (nr << 16)};
+  }
+}
+
+// grid (n_idx_tiles, h_k), block kIdxThreads; dynamic smem (idx_tok / 32) * nb_max
+// words: bit (t % 32) of word [t / 32][gb] is set when tile token t kept block gb.
+template <int TP>
+__global__ void __launch_bounds__(kIdxThreads) scatter_kernel(Params p) {
+  extern __shared__ uint32_t masks[];
+  const int nb = *p.nb;
+  const int h = blockIdx.y, tile = blockIdx.x, tid = threadIdx.x;
+  const int mw = p.idx_tok >> 5;
+  for (int i = tid; i < mw * nb; i += blockDim.x) masks[i] = 0u;
+  __syncthreads();
+  const int t = tile * p.idx_tok + tid;
+  const bool live = tid < p.idx_tok && t < p.n;
+  int32_t kgb[TP];
+#pragma unroll
+  for (int k = 0; k < TP; ++k) kgb[k] = -1;
+  if (live && nb > 0) {
+    bool bad = false;   // raised by the count pass already
+    token_blocks<TP>(p, nb, h, t, kgb, bad);
+#pragma unroll
+    for (int k = 0; k < TP; ++k)
+      if (kgb[k] >= 0) atomicOr(&masks[(tid >> 5) * nb + kgb[k]], 1u << (tid & 31));
+  }
+  __syncthreads();
+  if (!live) return;
+  const int wl = tid >> 5;
+  const uint32_t below = (1u << (tid & 31)) - 1u;
+  const int64_t hist_row = ((int64_t)h * p.n_idx_tiles + tile) * p.nb_max;
+  const int w = tile / p.wave_tiles;
+  const int64_t lo_row = ((int64_t)h * p.n_idx_tiles + (int64_t)w * p.wave_tiles) * p.nb_max;
+  int32_t *slot = p.slot_map + ((int64_t)h * p.n + t) * p.topk;
+  int32_t *prow = p.prow + ((int64_t)h * p.n + t) * p.topk;
+#pragma unroll
+  for (int k = 0; k < TP; ++k) {
+    if (k >= p.topk) break;
+    const int gb = kgb[k];
+    if (gb < 0) {
+      slot[k] = -1;
+      prow[k] = -1;
+      continue;
+    }
+    int32_t r = __popc(masks[wl * nb + gb] & below);
+    for (int w2 = 0; w2 < wl; ++w2) r += __popc(masks[w2 * nb + gb]);
+    const int32_t rank = p.chunk_hist[hist_row + gb] + r;   // rank inside block gb's list
+    const int32_t pos = p.offsets[h * nb + gb] + rank;
+    p.q_list[pos] = t;
+    slot[k] = pos;
+    const int32_t lo = p.chunk_hist[lo_row + gb];
+    const int64_t sub = ((int64_t)h * p.n_w + w) * p.nb_max + gb;
+    prow[k] = p.wtile_off[sub] * kTileRows + (rank - lo) * p.g;
+  }
 }
 
 // ---------------------------------------------------------------------------
 // Host launcher
 // ---------------------------------------------------------------------------
+template <int TP>
+static void launch_count_scatter(const Params &p, bool scatter, dim3 grid, size_t smem,
+                                 cudaStream_t stream) {
+  if (scatter)
+    scatter_kernel<TP><<<grid, kIdxThreads, smem, stream>>>(p);
+  else
+    count_kernel<TP><<<grid, kIdxThreads, smem, stream>>>(p);
+}
+
+static void count_or_scatter(const Params &p, bool scatter, dim3 grid, size_t smem,
+                             cudaStream_t s) {
+  if (p.topk <= 1) launch_count_scatter<1>(p, scatter, grid, smem, s);
+  else if (p.topk <= 2) launch_count_scatter<2>(p, scatter, grid, smem, s);
+  else if (p.topk <= 4) launch_count_scatter<4>(p, scatter, grid, smem, s);
+  else if (p.topk <= 8) launch_count_scatter<8>(p, scatter, grid, smem, s);
+  else if (p.topk <= 16) launch_count_scatter<16>(p, scatter, grid, smem, s);
+  else launch_count_scatter<32>(p, scatter, grid, smem, s);
+}
+
+size_t index_count_smem(const Params &p) { return sizeof(int32_t) * p.nb_max; }
+size_t index_scatter_smem(const Params &p) { return sizeof(uint32_t) * (p.idx_tok / 32) * p.nb_max; }
+
 cudaError_t launch_index(const Params &p, cudaStream_t stream, void (*mark)(int, cudaStream_t, bool)) {
-  int tp = 1;
-  while (tp < p.topk) tp <<= 1;
   mark(0, stream, true);
   geometry_kernel<<<1, 1024, 0, stream>>>(p);
   mark(0, stream, false);
-  const size_t smem = sizeof(int32_t) * p.idx_warps * p.nb_max;
-  dim3 grid_t(static_cast<unsigned>(p.n_idx_tiles), p.h_k);
+  const dim3 grid_t(static_cast<unsigned>(p.n_idx_tiles), p.h_k);
   mark(1, stream, true);
-  count_kernel<<<grid_t, p.idx_warps * 32, smem, stream>>>(p, tp);
+  count_or_scatter(p, false, grid_t, index_count_smem(p), stream);
   mark(1, stream, false);
   mark(2, stream, true);
   col_scan_kernel<<<dim3(static_cast<unsigned>((p.nb_max + 31) / 32), p.h_k), dim3(32, 8), 0,
@@ -274,19 +433,33 @@ cudaError_t launch_index(const Params &p, cudaStream_t stream, void (*mark)(int,
   mark(2, stream, false);
   mark(3, stream, true);
   scan_kernel<<<1, 1024, 0, stream>>>(p);
+  wave_scan_local_kernel<<<static_cast<unsigned>(p.n_scan_ctas), 1024, 0, stream>>>(p);
+  wave_scan_add_kernel<<<static_cast<unsigned>(p.n_scan_ctas), 1024, 0, stream>>>(p);
+  tile_desc_kernel<<<static_cast<unsigned>((p.nsub + 255) / 256), 256, 0, stream>>>(p);
   mark(3, stream, false);
   mark(4, stream, true);
-  scatter_kernel<<<grid_t, p.idx_warps * 32, smem, stream>>>(p, tp);
+  count_or_scatter(p, true, grid_t, index_scatter_smem(p), stream);
   mark(4, stream, false);
   return cudaGetLastError();
 }
 
-cudaError_t index_set_smem_limits(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+template <int TP>
+static cudaError_t set_limits_tp(int count_smem, int scatter_smem) {
+  cudaError_t e = cudaFuncSetAttribute(count_kernel<TP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, count_smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(smem));
+  return cudaFuncSetAttribute(scatter_kernel<TP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              scatter_smem);
+}
+
+cudaError_t index_set_smem_limits(const Params &p) {
+  const int cs = static_cast<int>(index_count_smem(p)), ss = static_cast<int>(index_scatter_smem(p));
+  if (p.topk <= 1) return set_limits_tp<1>(cs, ss);
+  if (p.topk <= 2) return set_limits_tp<2>(cs, ss);
+  if (p.topk <= 4) return set_limits_tp<4>(cs, ss);
+  if (p.topk <= 8) return set_limits_tp<8>(cs, ss);
+  if (p.topk <= 16) return set_limits_tp<16>(cs, ss);
+  return set_limits_tp<32>(cs, ss);
 }
 
 }  // namespace nsa
