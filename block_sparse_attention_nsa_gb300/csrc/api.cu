@@ -91,6 +91,14 @@ nsa_status check_dims(const nsa_sel_attn_dims *d, bool bwd) {
   return NSA_OK;
 }
 
+// Forward schedule: chunks of kFwdChunk consecutive tiles dealt round-robin to
+// the CTAs, so that all CTAs work on neighbouring (head, block) segments at any
+// time and the Q rows and K/V blocks they read stay L2-resident.
+#ifndef NSA_FWD_CHUNK
+#define NSA_FWD_CHUNK 8
+#endif
+constexpr int kFwdChunk = NSA_FWD_CHUNK;
+
 // Shared memory the index builder may use per CTA (count: one int per block;
 // scatter: one bit per (token, block) of the CTA's token tile).
 constexpr int64_t kIdxSmemCap = 160 * 1024;
@@ -104,9 +112,14 @@ nsa_status make_layout(const nsa_sel_attn_dims *d, Layout *L) {
   L->max_tiles = (L->max_rows + kTileRows - 1) / kTileRows + h_k * L->nb_max;
   L->max_chunks = (L->max_tiles + kBwdChunkTiles - 1) / kBwdChunkTiles + h_k * L->nb_max;
   if (L->nb_max * 4 > kIdxSmemCap) return NSA_ERR_UNSUPPORTED;
+  // scatter: token masks (1 bit), warp prefixes (1 byte) and two bases per block,
+  // plus the tile's slot_map and prow rows
+  auto scatter_bytes = [&](int tok) {
+    return (tok / 32) * L->nb_max * 5 + 2 * L->nb_max * 4 + 2 * (int64_t)tok * T * 4 + 16;
+  };
   int tok = kIdxThreads;
-  while (tok > 32 && (tok / 32) * L->nb_max * 4 > kIdxSmemCap) tok >>= 1;
-  if ((tok / 32) * L->nb_max * 4 > kIdxSmemCap) return NSA_ERR_UNSUPPORTED;
+  while (tok > 32 && scatter_bytes(tok) > kIdxSmemCap) tok >>= 1;
+  if (scatter_bytes(tok) > kIdxSmemCap) return NSA_ERR_UNSUPPORTED;
   L->idx_tok = tok;
   L->n_idx_tiles = (N + tok - 1) / tok;
   if (L->n_idx_tiles < 1) L->n_idx_tiles = 1;
@@ -192,7 +205,7 @@ void fill_params(Params *p, const nsa_sel_attn_dims *d, const Layout &L, void *w
   p->idx_tok = L.idx_tok;
   p->n_w = L.n_w;
   p->wave_tiles = L.wave_tiles;
-  p->fwd_chunk = 0;
+  p->fwd_chunk = kFwdChunk;
   p->obuf = w + L.obuf;
   p->mlbuf = reinterpret_cast<float2 *>(w + L.mlbuf);
   p->dstat = reinterpret_cast<float *>(w + L.dstat);

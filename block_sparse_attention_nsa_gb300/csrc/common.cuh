@@ -221,6 +221,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *map, int c0,
+                                                 int c1, int c2, uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
+      "l"(pol)
+      : "memory");
+}
+
 // Four rows (r0..r3) of a 2-D tensor map with a one-row box, columns [col, col + box).
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int col, int r0,
                                             int r1, int r2, int r3, uint64_t *bar) {
@@ -257,6 +267,28 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                "r"(src_bytes)
+               : "memory");
+}
+// L2 eviction policies (createpolicy) for streaming stores and reused loads.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void *src, uint32_t src_bytes,
+                                                uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+               "l"(src), "r"(src_bytes), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_v2_hint(float2 *dst, float2 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(dst), "f"(v.x),
+               "f"(v.y), "l"(pol)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
@@ -312,6 +344,28 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int rows, int s) 
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int rows, int s) {
   return sdesc_sw128(tile + s * 2048, rows * 128, 1024);
 }
+
+// The same descriptors split into their two 32-bit words, for kernels that keep
+// the constant upper word and the stage base of the lower word in registers and
+// step through k by adding to the 14-bit address field (addresses < 256 KB, so
+// the field never carries into the leading-byte-offset field).
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint32_t sdesc_lo_sw128(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t sdesc_join(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+// Byte offset of k-step s inside a K-major (rows x K) 128-byte-swizzled tile,
+// and inside an MN-major (K rows) tile, as used by desc_kmajor / desc_mnmajor.
+__host__ __device__ constexpr uint32_t kmajor_step(int rows, int s) {
+  return static_cast<uint32_t>((s >> 2) * rows * 128 + (s & 3) * 32);
+}
+__host__ __device__ constexpr uint32_t mnmajor_step(int s) { return static_cast<uint32_t>(s * 2048); }
 
 // Instruction descriptor, kind::f16: D = f32, A/B = bf16 (or f16), dense.
 __host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool a_mn, bool b_mn, bool fp16) {
@@ -392,6 +446,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 64 consecutive fp32 TMEM columns of this thread's lane, one wait for all.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]),
+        "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+        "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+        "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]),
+        "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 16 consecutive 32-bit TMEM columns of this thread's lane (a warp writes its
 // 32-lane subpartition); the caller waits with tmem_wait_st before signalling.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -414,6 +495,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
       "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
       "r"(c0), "r"(c1), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, uint32_t src, int c0,
+                                                  int c1, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%1, %2}], [%3], %4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(src), "l"(pol)
       : "memory");
 }
 __device__ __forceinline__ void bulk_wait_read_le1() {

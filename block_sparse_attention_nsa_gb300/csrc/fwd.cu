@@ -28,30 +28,36 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Pipeline depths per (d, B_K), bounded by 227 KB of shared memory: Q stages and
-// K/V stages.  Two output staging slots (one per softmax warpgroup) of one
-// 64-column block each.  TMEM (512 columns): two S slots of B_K columns (P, in
-// 16 bits, overwrites the first B_K / 2 columns of its S slot) and OS fp32 O
-// accumulators of d columns.
+// Pipeline depths per (d, B_K), bounded by 227 KB of shared memory: Q stages,
+// K/V stages and output staging slots per softmax warpgroup (one 64-column block
+// of 128 rows each; two let a warpgroup fill one while the TMA store of the other
+// drains).  TMEM (512 columns): two S slots of B_K columns (P, in 16 bits,
+// overwrites the first B_K / 2 columns of its S slot) and OS fp32 O accumulators
+// of d columns.
 __host__ __device__ constexpr int fwd_qs(int d, int bk) {
-  return d == 64 ? 4 : (d == 128 ? (bk == 128 ? 2 : 4) : (bk == 128 ? 1 : 2));
+  return d == 64 ? 4 : (d == 128 ? 4 : (bk == 128 ? 1 : 2));
 }
 __host__ __device__ constexpr int fwd_kvs(int d, int bk) {
-  return d == 256 ? (bk <= 32 ? 2 : 1) : 2;
+  return d == 64 ? 2 : (d == 128 ? (bk == 128 ? 1 : 2) : (bk <= 32 ? 2 : 1));
 }
+__host__ __device__ constexpr int fwd_ss(int d) { return d == 64 ? 2 : 1; }
 __host__ __device__ constexpr int fwd_os(int d, int bk) { return 2 * bk + 2 * d <= 512 ? 2 : 1; }
 
 template <int D, int BK>
 struct FwdSmem {
-  static constexpr int QS = fwd_qs(D, BK), KVS = fwd_kvs(D, BK), OS = fwd_os(D, BK);
+  static constexpr int QS = fwd_qs(D, BK), KVS = fwd_kvs(D, BK), SS = fwd_ss(D),
+                       OS = fwd_os(D, BK);
+  static constexpr int NPW = QS < 4 ? QS : 4;   // Q producer warps (one per stage or more)
+  static_assert(QS % NPW == 0, "each Q stage needs a single producer warp");
   static constexpr uint32_t kQ = 128u * D * 2u;            // one Q stage
   static constexpr uint32_t kK = uint32_t(BK) * D * 2u;     // one K (or V) stage
-  static constexpr uint32_t kStg = 128u * 64u * 2u;         // one staging slot
+  static constexpr uint32_t kStg = 128u * 64u * 2u;         // staging of one warpgroup
+  static constexpr uint32_t kStgW = 32u * 64u * 2u;         // one warp's staging slot
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kOffQ + QS * kQ;
   static constexpr uint32_t kOffV = kOffK + KVS * kK;
   static constexpr uint32_t kOffStg = kOffV + KVS * kK;
-  static constexpr uint32_t kBytes = kOffStg + 2 * kStg + 1024;   // + alignment slack
+  static constexpr uint32_t kBytes = kOffStg + 2 * SS * kStg + 1024;   // + alignment slack
   static_assert(kBytes <= 227u * 1024u, "shared memory budget");
   static_assert(2 * BK + OS * D <= 512, "TMEM budget");
   static constexpr uint32_t kTmemCols = 512;
@@ -88,10 +94,12 @@ __device__ __forceinline__ TileDesc load_desc(const Params &p, const TileSeq &s)
 }
 
 // Persistent, warp-specialised forward main kernel (one CTA per SM).
-//   warps 0-3: producer -- the gathered Q rows of each tile by cp.async (16-byte
-//     chunks, a warp instruction covering 256 / d whole rows, so reads are fully
-//     coalesced), written into the 128-byte-swizzled operand layout.  A Q stage
-//     is released as soon as the S MMA that reads it completes;
+//   warps 0-3: producers (as many as Q stages, at most 4) -- warp w gathers the
+//     Q rows of tiles w, w + NPW, ... by
+//     cp.async (16-byte chunks, a warp instruction covering 256 / d whole rows,
+//     so reads are fully coalesced) into the 128-byte-swizzled operand layout,
+//     waits for its own copies and arrives; a Q stage is released as soon as the
+//     S MMA that reads it completes;
 //   warp 6 (one thread): K_b and V_b by TMA (3-D tensor maps, once per change of
 //     (KV head, block));
 //   warp 4 (one thread): tcgen05 MMAs S(i) = Q K^T into TMEM slot i % 2 and
@@ -130,7 +138,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (warp == 5) tmem_alloc(&tmem_base, L::kTmemCols);
   if (tid == 0) {
-    for (int i = 0; i < QS; ++i) { mbar_init(&q_full[i], 128); mbar_init(&q_empty[i], 1); }
+    for (int i = 0; i < QS; ++i) { mbar_init(&q_full[i], 32); mbar_init(&q_empty[i], 1); }
     for (int i = 0; i < KVS; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -147,80 +155,89 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tS0 = tmem_base, tO0 = tmem_base + 2 * BK;
   const int total = p.wtile_off[p.nsub];
 
-  if (warp < 4) {
+  if (warp < L::NPW) {
     // ------------------------------ producer ------------------------------
+    // Warp w gathers whole tiles w, w + NPW, w + 2 NPW, ... of this CTA: it waits
+    // for its own copies of a tile, fences them for the tensor core and arrives,
+    // so a tile's readiness never depends on the issue of later tiles.  NPW
+    // divides QS, so every Q stage has exactly one producer warp and no waiter on
+    // a stage's barriers can run two phases ahead.
+    constexpr int NPW = L::NPW;
     constexpr int kCPR = D / 8;           // 16-byte chunks per row
     constexpr int kRPI = 32 / kCPR;       // rows per warp instruction
-    constexpr int kLag = QS - 1;          // tiles whose copies stay in flight
-    const int pt = tid, pw = pt >> 5;
+    constexpr int kIns = 128 / kRPI;      // warp instructions per tile
     TileSeq seq;
     seq.init(total, p.fwd_chunk);
+    for (int k = 0; k < warp; ++k) seq.next();
     const int oob_row = p.n * p.h_q;
-    // global Q row of tile row 32 pw + lane (oob_row for padding rows)
-    auto row_id = [&](const TileDesc &d) {
-      const int h = d.hn & 0xffff, nrows = d.hn >> 16, r = pw * 32 + lane;
-      if (r >= nrows) return oob_row;
-      const int rr = d.row0 + r;
-      const int t = __ldg(p.q_list + d.q_off + rr / p.g);
-      return t * p.h_q + h * p.g + rr % p.g;
+    // rid[j] = global Q row of tile row 32 j + lane (oob_row for padding rows)
+    auto tile_rids = [&](const TileDesc &d, int (&rid)[4]) {
+      const int h = d.hn & 0xffff, nrows = d.hn >> 16;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = j * 32 + lane;
+        rid[j] = oob_row;
+        if (r < nrows) {
+          const int rr = d.row0 + r;
+          const int t = __ldg(p.q_list + d.q_off + rr / p.g);
+          rid[j] = t * p.h_q + h * p.g + rr % p.g;
+        }
+      }
+    };
+    auto same_kv = [](const TileDesc &a, const TileDesc &b) {
+      return (a.hn & 0xffff) == (b.hn & 0xffff) && a.key0 == b.key0;
     };
     const uint16_t *gq = static_cast<const uint16_t *>(p.q);
-    int li = 0, kv_n = 0, prev_h = -1, prev_key0 = -1;
-    TileDesc dc = load_desc(p, seq);
-    TileSeq seq1 = seq;
-    seq1.next();
-    TileDesc dn = load_desc(p, seq1);
-    int rid_c = seq.valid() ? row_id(dc) : oob_row;
+    const uint64_t keep = l2_evict_last();    // Q rows are gathered ~T times each
+    int li = warp;
+    // prv = the tile before this warp's current one in the CTA's sequence
+    TileSeq prv;
+    prv.init(total, p.fwd_chunk);
+    for (int k = 0; k + 1 < warp; ++k) prv.next();
     while (seq.valid()) {
-      TileSeq seq2 = seq1;
-      seq2.next();
-      const TileDesc dnn = load_desc(p, seq2);               // two tiles ahead
-      const int rid_n = seq1.valid() ? row_id(dn) : oob_row;  // one tile ahead
-      // K/V flags of this tile for the MMA thread (the loads are warp 6's)
-      const int h = dc.hn & 0xffff;
-      const bool first = h != prev_h || dc.key0 != prev_key0;
-      const bool last = !seq1.valid() || (dn.hn & 0xffff) != h || dn.key0 != dc.key0;
-      if (first) {
-        ++kv_n;
-        prev_h = h;
-        prev_key0 = dc.key0;
-      }
+      const TileDesc dc = load_desc(p, seq);
+      TileSeq sn = seq;
+      sn.next();
+      const TileDesc dn = load_desc(p, sn);
+      const TileDesc dp = li > 0 ? load_desc(p, prv) : TileDesc{0, 0, -1, -1};
+      int rid[4];
+      tile_rids(dc, rid);
+      const bool first = li == 0 || !same_kv(dp, dc);
+      const bool last = !sn.valid() || !same_kv(dn, dc);
       const int qs = li % QS;
       if (li >= QS) mbar_wait_sticky(&q_empty[qs], ((li / QS) - 1) & 1, p.status, &fail);
-      if (pt == 0)
-        q_flags[qs] = static_cast<uint32_t>((kv_n - 1) % KVS) | (first ? 0x100u : 0u) |
-                      (last ? 0x200u : 0u);
       const uint32_t stage = sQ0 + qs * L::kQ;
 #pragma unroll
-      for (int ins = 0; ins < kCPR; ++ins) {
-        const int src_lane = ins * kRPI + lane / kCPR;
-        const int rid = __shfl_sync(0xffffffffu, rid_c, src_lane);
-        const int chunk = lane % kCPR;
-        const bool in = rid < oob_row;
-        cp_async16(stage + sw128_offset(pw * 32 + src_lane, chunk, 128),
-                   gq + (in ? (int64_t)rid * D + chunk * 8 : 0), in ? 16u : 0u);
+      for (int j = 0; j < 4; ++j) {              // tile rows 32 j .. 32 j + 31
+#pragma unroll 4
+        for (int k = 0; k < kIns / 4; ++k) {
+          const int r = (j * (kIns / 4) + k) * kRPI + lane / kCPR;   // this lane's row
+          const int id = __shfl_sync(0xffffffffu, rid[j], r & 31);
+          const int chunk = lane % kCPR;
+          const bool in = id < oob_row;
+          cp_async16_hint(stage + sw128_offset(r, chunk, 128),
+                          gq + (in ? (int64_t)id * D + chunk * 8 : 0), in ? 16u : 0u, keep);
+        }
       }
       cp_async_commit();
-      if (li >= kLag) {
-        cp_async_wait_group<kLag>();
-        fence_proxy_async_smem();
-        mbar_arrive(&q_full[(li - kLag) % QS]);
-      }
-      ++li;
-      seq = seq1;
-      seq1 = seq2;
-      dc = dn;
-      dn = dnn;
-      rid_c = rid_n;
+      if (lane == 0) q_flags[qs] = (first ? 0x100u : 0u) | (last ? 0x200u : 0u);
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      mbar_arrive(&q_full[qs]);
+      // next tile of this warp: li + NPW; its predecessor is li + NPW - 1
+      prv = seq;
+#pragma unroll
+      for (int k = 0; k + 1 < NPW; ++k) prv.next();
+      seq = prv;
+      seq.next();
+      li += NPW;
     }
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-    for (int j = li - kLag > 0 ? li - kLag : 0; j < li; ++j) mbar_arrive(&q_full[j % QS]);
   } else if (warp == 6) {
     // --------------------------- K/V producer -----------------------------
     // A warp of its own: its waits on kv_empty must not hold back the Q
     // producers, whose q_full arrivals lag their copies by QS - 1 tiles.
     if (lane == 0) {
+      const uint64_t keep = l2_evict_last();    // a block's K/V serve all its tiles
       TileSeq seq;
       seq.init(total, p.fwd_chunk);
       int kv_n = 0, prev_h = -1, prev_key0 = -1;
@@ -240,8 +257,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mbar_arrive_expect_tx(&kv_full[ks], 2u * L::kK);
 #pragma unroll
           for (int cb = 0; cb < kCB; ++cb) {
-            tma_load_3d(sK0 + ks * L::kK + cb * BK * 128, &tm_k, cb * 64, h, dc.key0, &kv_full[ks]);
-            tma_load_3d(sV0 + ks * L::kK + cb * BK * 128, &tm_v, cb * 64, h, dc.key0, &kv_full[ks]);
+            tma_load_3d_hint(sK0 + ks * L::kK + cb * BK * 128, &tm_k, cb * 64, h, dc.key0,
+                             &kv_full[ks], keep);
+            tma_load_3d_hint(sV0 + ks * L::kK + cb * BK * 128, &tm_v, cb * 64, h, dc.key0,
+                             &kv_full[ks], keep);
           }
           ++kv_n;
           prev_h = h;
@@ -260,7 +279,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       seq.init(total, p.fwd_chunk);
       int n = 0;    // tiles of this CTA
       for (TileSeq c = seq; c.valid(); c.next()) ++n;
+      // descriptor words: constant upper words, per-stage lower words
+      constexpr uint32_t kHiK = sdesc_hi_sw128(1024);   // K-major Q, K and MN-major V
+      uint32_t lo_q[QS], lo_k[KVS], lo_v[KVS];
+#pragma unroll
+      for (int j = 0; j < QS; ++j) lo_q[j] = sdesc_lo_sw128(sQ0 + j * L::kQ, 16);
+#pragma unroll
+      for (int j = 0; j < KVS; ++j) {
+        lo_k[j] = sdesc_lo_sw128(sK0 + j * L::kK, 16);
+        lo_v[j] = sdesc_lo_sw128(sV0 + j * L::kK, BK * 128);
+      }
       uint32_t flags[2] = {0u, 0u};   // K/V flags of tiles i and i + 1 (index i & 1)
+      int kvs[2] = {0, 0};            // K/V stage of tiles i and i + 1
       int s_next = 0;                 // next tile whose S has to be issued
       int s_kv = 0;                   // K/V loads consumed so far (load m fills stage m % KVS)
       auto issue_s = [&]() {
@@ -268,35 +298,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_wait_sticky(&q_full[qs], (i / QS) & 1, p.status, &fail);
         const uint32_t f = q_flags[qs];
         flags[i & 1] = f;
-        const int ks = static_cast<int>(f & 0xffu);
         if (f & 0x100u) {
-          // load s_kv is the (s_kv / KVS)-th fill of stage s_kv % KVS (== ks)
-          mbar_wait_sticky(&kv_full[ks], (s_kv / KVS) & 1, p.status, &fail);
+          // load s_kv is the (s_kv / KVS)-th fill of stage s_kv % KVS
+          mbar_wait_sticky(&kv_full[s_kv % KVS], (s_kv / KVS) & 1, p.status, &fail);
           ++s_kv;
         }
+        const int ks = (s_kv - 1) % KVS;
+        kvs[i & 1] = ks;
         tc_fence_after();
+        uint32_t aq = lo_q[0], bk = lo_k[0];
+#pragma unroll
+        for (int j = 1; j < QS; ++j) aq = qs == j ? lo_q[j] : aq;
+#pragma unroll
+        for (int j = 1; j < KVS; ++j) bk = ks == j ? lo_k[j] : bk;
+        const uint32_t tSd = tS0 + (i & 1) * BK;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_f16(tS0 + (i & 1) * BK, desc_kmajor(sQ0 + qs * L::kQ, 128, kk),
-                  desc_kmajor(sK0 + ks * L::kK, BK, kk), kIdescS, kk > 0);
+          mma_f16(tSd, sdesc_join(aq + (kmajor_step(128, kk) >> 4), kHiK),
+                  sdesc_join(bk + (kmajor_step(BK, kk) >> 4), kHiK), kIdescS, kk > 0);
         mma_commit(&s_full[i & 1]);
         mma_commit(&q_empty[qs]);
         ++s_next;
       };
       for (int i = 0; i < n; ++i) {
         if (s_next == i) issue_s();
-        // S(i + 1) goes ahead of O(i) unless its K/V stage is only released by O(i)
-        // itself (a single K/V stage and a change of block after tile i).
-        if (s_next == i + 1 && i + 1 < n && !(KVS == 1 && (flags[i & 1] & 0x200u))) issue_s();
+        // S(i + 1) goes ahead of O(i) when its Q rows are already in and its K/V
+        // stage is not one that only O(i) releases (a single K/V stage and a
+        // change of block after tile i)
+        if (s_next == i + 1 && i + 1 < n && !(KVS == 1 && (flags[i & 1] & 0x200u)) &&
+            mbar_try_wait(smem_u32(&q_full[(i + 1) % QS]), ((i + 1) / QS) & 1))
+          issue_s();
         const uint32_t f = flags[i & 1];
-        const int ks = static_cast<int>(f & 0xffu), os = i % OS;
+        const int ks = kvs[i & 1], os = i % OS;
         mbar_wait_sticky(&p_full[i & 1], (i >> 1) & 1, p.status, &fail);
         if (i >= OS) mbar_wait_sticky(&o_free[os], ((i / OS) - 1) & 1, p.status, &fail);
         tc_fence_after();
-        const uint32_t tP = tS0 + (i & 1) * BK;
+        const uint32_t tP = tS0 + (i & 1) * BK, tOd = tO0 + os * D;
+        uint32_t bv = lo_v[0];
+#pragma unroll
+        for (int j = 1; j < KVS; ++j) bv = ks == j ? lo_v[j] : bv;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          mma_f16_ts(tO0 + os * D, tP + kk * 8, desc_mnmajor(sV0 + ks * L::kK, BK, kk), kIdescO,
+          mma_f16_ts(tOd, tP + kk * 8, sdesc_join(bv + (mnmajor_step(kk) >> 4), kHiK), kIdescO,
                      kk > 0);
         mma_commit(&o_full[i & 1]);
         if (f & 0x200u) mma_commit(&kv_empty[ks]);
@@ -307,96 +350,168 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int wg = (warp - 8) >> 2;
     const int row = tid - 256 - wg * 128;                  // tile row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t stg = sStg0 + wg * L::kStg;
+    constexpr int SS = L::SS;
+    const uint32_t stg = sStg0 + (warp - 8) * SS * L::kStgW;
+    const uint64_t stream = l2_evict_first();   // partials are read once, by the merge
     TileSeq seq;
     seq.init(total, p.fwd_chunk);
     if (wg == 1) seq.next();
+    // descriptor and causal limit of this warpgroup's next tile, loaded one tile early
+    auto tile_lim = [&](const TileDesc &d) {
+      const int nrows = d.hn >> 16;
+      if (row >= nrows) return -1;
+      const int t = __ldg(p.q_list + d.q_off + (d.row0 + row) / p.g);
+      return min(BK - 1, t - d.key0);
+    };
+    TileDesc dsc = load_desc(p, seq);
+    int lim = seq.valid() ? tile_lim(dsc) : -1;
+    TileSeq nseq = seq;
+    nseq.next();
+    nseq.next();
+    TileDesc ndsc = load_desc(p, nseq);
+    int n_cb = 0;                                 // column blocks stored so far
     for (int i = wg; seq.valid(); i += 2) {
       const int tile = seq.tile();
-      const TileDesc dsc = load_desc(p, seq);
       const int nrows = dsc.hn >> 16;
       const bool row_in = row < nrows;
-      int lim = -1;
-      if (row_in) {
-        const int t = __ldg(p.q_list + dsc.q_off + (dsc.row0 + row) / p.g);
-        lim = min(BK - 1, t - dsc.key0);
-      }
       const int os = i % OS;
       mbar_wait_sticky(&s_full[i & 1], (i >> 1) & 1, p.status, &fail);
       tc_fence_after();
       const uint32_t tS = tS0 + (i & 1) * BK + lane_off;
-      float mx = -INFINITY;
+      float lsum = 0.f, m2 = 0.f;
+      if constexpr (BK == 128) {
+        // two passes over 32-column chunks (128 scores do not stay in registers)
+        float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < BK / 32; ++c) {
-        float sv[32];
-        tmem_ld32(tS + c * 32, sv);
+        for (int c = 0; c < BK / 32; ++c) {
+          float sv[32];
+          tmem_ld32(tS + c * 32, sv);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c * 32 + j <= lim) mx = fmaxf(mx, sv[j]);
-      }
-      const float m2 = row_in ? mx * p.scale_log2 : 0.f;
-      float lsum = 0.f;
-#pragma unroll
-      for (int c = 0; c < BK / 32; ++c) {
-        float sv[32];
-        tmem_ld32(tS + c * 32, sv);
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const int ii = c * 32 + j;
-          const float p0 = (ii <= lim) ? ex2_approx(fmaf(sv[j], p.scale_log2, -m2)) : 0.f;
-          const float p1 = (ii + 1 <= lim) ? ex2_approx(fmaf(sv[j + 1], p.scale_log2, -m2)) : 0.f;
-          lsum += p0 + p1;                    // fp32 row sum (exact lse)
-          pk[j / 2] = pack2<kFp16>(p0, p1);   // P rounded to 16 bits for the PV MMA
+          for (int j = 0; j < 32; ++j)
+            if (c * 32 + j <= lim) mx = fmaxf(mx, sv[j]);
         }
-        // 32 P values of this chunk -> 16 TMEM columns; they overwrite S columns
-        // [16 c, 16 c + 16), which this thread has already read.
-        tmem_st16(tS + c * 16, pk);
+        m2 = row_in ? mx * p.scale_log2 : 0.f;
+#pragma unroll
+        for (int c = 0; c < BK / 32; ++c) {
+          float sv[32];
+          tmem_ld32(tS + c * 32, sv);
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int ii = c * 32 + j;
+            const float p0 = (ii <= lim) ? ex2_approx(fmaf(sv[j], p.scale_log2, -m2)) : 0.f;
+            const float p1 = (ii + 1 <= lim) ? ex2_approx(fmaf(sv[j + 1], p.scale_log2, -m2)) : 0.f;
+            lsum += p0 + p1;                    // fp32 row sum (exact lse)
+            pk[j / 2] = pack2<kFp16>(p0, p1);   // P rounded to 16 bits for the PV MMA
+          }
+          // 32 P values of this chunk -> 16 TMEM columns; they overwrite S columns
+          // [16 c, 16 c + 16), which this thread has already read.
+          tmem_st16(tS + c * 16, pk);
+        }
+      } else {
+        // all B_K scores of the row in registers: one TMEM load, one wait
+        float sv[BK];
+        if constexpr (BK == 64) {
+          tmem_ld64(tS, sv);
+        } else {
+          tmem_ld32(tS, sv);
+        }
+        // Only rows of a tile of the token's own block need the causal mask; a
+        // warp whose rows all see the whole block takes the unmasked path.
+        // Eight independent max / sum chains keep the dependent latency short.
+        const bool full = __all_sync(0xffffffffu, !row_in || lim >= BK - 1);
+        float mxs[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
+        if (full) {
+#pragma unroll
+          for (int j = 0; j < BK; ++j) mxs[j & 7] = fmaxf(mxs[j & 7], sv[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < BK; ++j)
+            if (j <= lim) mxs[j & 7] = fmaxf(mxs[j & 7], sv[j]);
+        }
+        const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                               fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+        m2 = row_in ? mx * p.scale_log2 : 0.f;
+        float ls[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ls[j] = 0.f;
+#pragma unroll
+        for (int c = 0; c < BK / 32; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int ii = c * 32 + j;
+            float p0 = ex2_approx(fmaf(sv[ii], p.scale_log2, -m2));
+            float p1 = ex2_approx(fmaf(sv[ii + 1], p.scale_log2, -m2));
+            if (!full) {
+              p0 = (ii <= lim) ? p0 : 0.f;
+              p1 = (ii + 1 <= lim) ? p1 : 0.f;
+            }
+            ls[(j >> 1) & 7] += p0 + p1;        // fp32 row sum (exact lse)
+            pk[j / 2] = pack2<kFp16>(p0, p1);   // P rounded to 16 bits for the PV MMA
+          }
+          tmem_st16(tS + c * 16, pk);         // overwrites S columns already read
+        }
+        lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[i & 1]);
+      // the next tile's causal limit: its q_list read overlaps this epilogue
+      const int nlim = nseq.valid() ? tile_lim(ndsc) : -1;
 
-      // epilogue: O(i) -> 16-bit, one 64-column block at a time through this
-      // warpgroup's staging slot, TMA-stored to the tile's 128 compact-buffer rows
+      // epilogue: O(i) -> 16-bit, one 64-column block at a time; each warp stages
+      // its 32 rows in its own slots and TMA-stores them to the tile's
+      // compact-buffer rows, so no warpgroup-wide barrier is needed
       mbar_wait_sticky(&o_full[i & 1], (i >> 1) & 1, p.status, &fail);
       tc_fence_after();
 #pragma unroll
       for (int cb = 0; cb < kCB; ++cb) {
+        uint32_t pk[32];
+        {
+          float ov[64];
+          tmem_ld64(tO0 + os * D + cb * 64 + lane_off, ov);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float ov[32];
-          tmem_ld32(tO0 + os * D + cb * 64 + half * 32 + lane_off, ov);
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) pk[j / 2] = pack2<kFp16>(ov[j], ov[j + 1]);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const uint32_t so = sw128_offset(row, half * 4 + q4, 128);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg + so),
-                         "r"(pk[q4 * 4]), "r"(pk[q4 * 4 + 1]), "r"(pk[q4 * 4 + 2]),
-                         "r"(pk[q4 * 4 + 3])
-                         : "memory");
-          }
+          for (int j = 0; j < 64; j += 2) pk[j / 2] = pack2<kFp16>(ov[j], ov[j + 1]);
         }
         if (cb == kCB - 1) {
           tc_fence_before();
           mbar_arrive(&o_free[os]);
         }
-        fence_proxy_async_smem();
-        named_bar_sync(1 + wg, 128);
-        if (row == 0) {
-          tma_store_2d(&tm_o, stg, cb * 64, tile * kTileRows);
-          bulk_commit();
-          bulk_wait_read_all();   // the slot is rewritten by the next column block
+        const uint32_t slot = stg + (n_cb % SS) * L::kStgW;
+        // the slot's previous TMA store (this lane 0's bulk group) must have been read
+        if (lane == 0 && n_cb >= SS) {
+          if constexpr (SS == 2) bulk_wait_read_le1();
+          else bulk_wait_read_all();
         }
-        named_bar_sync(1 + wg, 128);
+        __syncwarp();
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const uint32_t so = sw128_offset(lane, q4, 32);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + so),
+                       "r"(pk[q4 * 4]), "r"(pk[q4 * 4 + 1]), "r"(pk[q4 * 4 + 2]),
+                       "r"(pk[q4 * 4 + 3])
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d_hint(&tm_o, slot, cb * 64, tile * kTileRows + (warp & 3) * 32, stream);
+          bulk_commit();
+        }
+        ++n_cb;
       }
-      p.mlbuf[(int64_t)tile * kTileRows + row] = make_float2(m2, lsum);
-      seq.next();
-      seq.next();
+      st_global_v2_hint(p.mlbuf + (int64_t)tile * kTileRows + row, make_float2(m2, lsum), stream);
+      seq = nseq;
+      dsc = ndsc;
+      lim = nlim;
+      nseq.next();
+      nseq.next();
+      ndsc = load_desc(p, nseq);
     }
-    if (row == 0) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -432,27 +547,36 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(Params p) {
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   const uint16_t *obuf = static_cast<const uint16_t *>(p.obuf);
-  for (int kk = 0; kk < p.topk; ++kk) {
-    const int64_t r = __shfl_sync(0xffffffffu, row, kk);
-    const float wk = __shfl_sync(0xffffffffu, w, kk);
-    if (r < 0) continue;
-    const uint16_t *src = obuf + r * D + lane * E;
-    uint32_t u[E / 2];
-    if constexpr (E == 2) {
-      u[0] = *reinterpret_cast<const uint32_t *>(src);
-    } else if constexpr (E == 4) {
-      const uint2 x = *reinterpret_cast<const uint2 *>(src);
-      u[0] = x.x; u[1] = x.y;
-    } else {
-      const uint4 x = *reinterpret_cast<const uint4 *>(src);
-      u[0] = x.x; u[1] = x.y; u[2] = x.z; u[3] = x.w;
+  // eight partial rows in flight per lane before any is consumed
+  constexpr int kBatch = 8;
+  for (int k0 = 0; k0 < p.topk; k0 += kBatch) {
+    uint32_t u[kBatch][E / 2];
+    float wk[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t r = __shfl_sync(0xffffffffu, row, (k0 + b) & 31);
+      wk[b] = __shfl_sync(0xffffffffu, w, (k0 + b) & 31);
+      const bool ok = k0 + b < p.topk && r >= 0;
+      if (!ok) wk[b] = 0.f;
+      const uint16_t *src = obuf + (ok ? r : 0) * D + lane * E;
+      if constexpr (E == 2) {
+        u[b][0] = ok ? *reinterpret_cast<const uint32_t *>(src) : 0u;
+      } else if constexpr (E == 4) {
+        const uint2 x = ok ? *reinterpret_cast<const uint2 *>(src) : make_uint2(0u, 0u);
+        u[b][0] = x.x; u[b][1] = x.y;
+      } else {
+        const uint4 x = ok ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0u, 0u, 0u, 0u);
+        u[b][0] = x.x; u[b][1] = x.y; u[b][2] = x.z; u[b][3] = x.w;
+      }
     }
 #pragma unroll
-    for (int e = 0; e < E / 2; ++e) {
-      const float2 f = unpack2<kFp16>(u[e]);
-      acc[2 * e] = fmaf(wk, f.x, acc[2 * e]);
-      acc[2 * e + 1] = fmaf(wk, f.y, acc[2 * e + 1]);
-    }
+    for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+      for (int e = 0; e < E / 2; ++e) {
+        const float2 f = unpack2<kFp16>(u[b][e]);
+        acc[2 * e] = fmaf(wk[b], f.x, acc[2 * e]);
+        acc[2 * e + 1] = fmaf(wk[b], f.y, acc[2 * e + 1]);
+      }
   }
   const bool any = lsum > 0.f;
   const float inv = any ? 1.f / lsum : 0.f;
@@ -512,12 +636,12 @@ bool make_qkv_maps(const Params &p, const void *q, CUtensorMap *mq, CUtensorMap 
 }
 
 // Tensor map of the compact partial buffer: [max_tiles * 128 rows, d], box =
-// 128 rows x 64 columns, 128-byte swizzle (the staging slot's layout).
+// 32 rows x 64 columns (one warp's rows), 128-byte swizzle (the staging layout).
 static bool make_obuf_map(const Params &p, int64_t max_tiles, CUtensorMap *mo) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.d),
                               static_cast<cuuint64_t>(max_tiles) * kTileRows};
   const cuuint64_t str[1] = {static_cast<cuuint64_t>(p.d) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTileRows)};
+  const cuuint32_t box[2] = {64, 32};
   return encode_map(mo, p.dtype == NSA_FP16, 2, p.obuf, dims, str, box);
 }
 

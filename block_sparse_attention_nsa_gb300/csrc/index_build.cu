@@ -118,36 +118,56 @@ __global__ void __launch_bounds__(kIdxThreads) count_kernel(Params p) {
   for (int i = tid; i < nb; i += blockDim.x) bins[i] = 0;
   __syncthreads();
   const int t = tile * p.idx_tok + tid;
+  int32_t kgb[TP];
+#pragma unroll
+  for (int k = 0; k < TP; ++k) kgb[k] = -1;
   if (tid < p.idx_tok && t < p.n) {
-    int32_t kgb[TP];
     bool bad = false;
     int np = 0;
     if (nb > 0) {
       np = token_blocks<TP>(p, nb, h, t, kgb, bad);
-#pragma unroll
-      for (int k = 0; k < TP; ++k)
-        if (kgb[k] >= 0) atomicAdd(&bins[kgb[k]], 1);
     }
     if (bad) set_status(p.status, NSA_DEVERR_BAD_INDEX);
     p.npairs[(int64_t)h * p.n + t] = np;
+  }
+  {
+    // lanes naming the same block as their warp's lowest active lane in slot k
+    // (the own block and block 0, typically) add once for all of them
+    const bool live = tid < p.idx_tok && t < p.n && nb > 0;
+    const uint32_t act = __ballot_sync(0xffffffffu, live);
+    if (live) {
+      const int leader = __ffs(act) - 1;
+#pragma unroll
+      for (int k = 0; k < TP; ++k) {
+        const int32_t lead_gb = __shfl_sync(act, kgb[k], leader);
+        const uint32_t same = __ballot_sync(act, kgb[k] == lead_gb && kgb[k] >= 0);
+        if (kgb[k] >= 0) {
+          if (kgb[k] != lead_gb) atomicAdd(&bins[kgb[k]], 1);
+          else if ((tid & 31) == leader) atomicAdd(&bins[kgb[k]], __popc(same));
+        }
+      }
+    }
   }
   __syncthreads();
   int32_t *hist = p.chunk_hist + ((int64_t)h * p.n_idx_tiles + tile) * p.nb_max;
   for (int gb = tid; gb < nb; gb += blockDim.x) hist[gb] = bins[gb];
 }
 
-// grid (ceil(nb_max / 32), h_k), block (32, 8): exclusive prefix over token tiles
-__global__ void __launch_bounds__(256) col_scan_kernel(Params p) {
-  __shared__ int32_t part[8][33];
+// grid (ceil(nb_max / 32), h_k), block (32, 32): exclusive prefix over token tiles;
+// thread (x, y) covers block 32 * blockIdx.x + x and one range of token tiles.
+__global__ void __launch_bounds__(1024) col_scan_kernel(Params p) {
+  __shared__ int32_t part[32][33];
   const int nb = *p.nb;
   const int gb = blockIdx.x * 32 + threadIdx.x, h = blockIdx.y, y = threadIdx.y;
   const int64_t T = p.n_idx_tiles;
-  const int64_t per = (T + 7) / 8;
+  const int64_t per = (T + 31) / 32;
   const int64_t t0 = min(T, y * per), t1 = min(T, t0 + per);
   int32_t *col = p.chunk_hist + (int64_t)h * T * p.nb_max + gb;
   int32_t local = 0;
-  if (gb < nb)
+  if (gb < nb) {
+#pragma unroll 8
     for (int64_t t = t0; t < t1; ++t) local += col[t * p.nb_max];
+  }
   part[y][threadIdx.x] = local;
   __syncthreads();
   int32_t run = 0;
@@ -158,7 +178,7 @@ __global__ void __launch_bounds__(256) col_scan_kernel(Params p) {
       col[t * p.nb_max] = run;
       run += c;
     }
-    if (y == 7) p.counts[h * nb + gb] = run;
+    if (y == 31) p.counts[h * nb + gb] = run;
   }
 }
 
@@ -321,10 +341,11 @@ __global__ void __launch_bounds__(1024) wave_scan_add_kernel(Params p) {
     p.wtile_off[p.nsub] = b + p.wscan_part[blockIdx.x];
 }
 
-// One thread per sub-segment: writes the descriptors of its tiles.
+// One warp per sub-segment: lane j writes the descriptors of tiles j, j + 32, ...
 __global__ void __launch_bounds__(256) tile_desc_kernel(Params p) {
   const int nb = *p.nb;
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
   if (i >= p.nsub) return;
   const int32_t t0 = p.wtile_off[i], nt = p.wtile_off[i + 1] - t0;
   if (nt <= 0) return;
@@ -335,24 +356,50 @@ __global__ void __launch_bounds__(256) tile_desc_kernel(Params p) {
   const int s = upper_index(p.blk_start, p.num_seqs + 1, gb);
   const int32_t key0 = p.cu[s] + (gb - p.blk_start[s]) * p.block;
   const int32_t q_off = p.offsets[h * nb + gb] + lo;
-  for (int j = 0; j < nt; ++j) {
+  for (int j = lane; j < nt; j += 32) {
     const int64_t left = rows - (int64_t)j * kTileRows;
     const int32_t nr = static_cast<int32_t>(left < kTileRows ? left : kTileRows);
     p.tdesc[t0 + j] = TileDesc{q_off, j * kTileRows, key0, h | (nr << 16)};
   }
 }
 
-// grid (n_idx_tiles, h_k), block kIdxThreads; dynamic smem (idx_tok / 32) * nb_max
-// words: bit (t % 32) of word [t / 32][gb] is set when tile token t kept block gb.
+// grid (n_idx_tiles, h_k), block kIdxThreads; dynamic smem, in 32-bit words:
+//   masks [idx_tok / 32][nb_max]: bit (t % 32) of word [t / 32][gb] is set when tile
+//                                 token t kept block gb;
+//   qbase, pbase [nb_max]:        the block's first q_list position and first
+//                                 forward partial row for this tile's tokens;
+//   wpre [idx_tok / 32][nb_max]:  bytes, tokens of earlier warps that kept gb;
+//   rows [2][idx_tok * T]:        this tile's slot_map and prow rows, written out
+//                                 with coalesced stores.
+size_t index_scatter_smem(const Params &p) {
+  const size_t mw = p.idx_tok / 32;
+  return 4 * (mw * p.nb_max + 2 * p.nb_max + 2 * (size_t)p.idx_tok * p.topk) + mw * p.nb_max + 16;
+}
+
 template <int TP>
 __global__ void __launch_bounds__(kIdxThreads) scatter_kernel(Params p) {
   extern __shared__ uint32_t masks[];
   const int nb = *p.nb;
-  const int h = blockIdx.y, tile = blockIdx.x, tid = threadIdx.x;
+  const int h = blockIdx.y, tile = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const int mw = p.idx_tok >> 5;
+  int32_t *qbase = reinterpret_cast<int32_t *>(masks + mw * p.nb_max);
+  int32_t *pbase = qbase + p.nb_max;
+  int32_t *srow = pbase + p.nb_max;                      // [idx_tok * T]
+  int32_t *prow_s = srow + (int64_t)p.idx_tok * p.topk;  // [idx_tok * T]
+  uint8_t *wpre = reinterpret_cast<uint8_t *>(prow_s + (int64_t)p.idx_tok * p.topk);
+  const int w = tile / p.wave_tiles;
+  const int64_t hist_row = ((int64_t)h * p.n_idx_tiles + tile) * p.nb_max;
+  const int64_t lo_row = ((int64_t)h * p.n_idx_tiles + (int64_t)w * p.wave_tiles) * p.nb_max;
+  const int64_t sub_row = ((int64_t)h * p.n_w + w) * p.nb_max;
   for (int i = tid; i < mw * nb; i += blockDim.x) masks[i] = 0u;
+  for (int gb = tid; gb < nb; gb += blockDim.x) {
+    const int32_t before = p.chunk_hist[hist_row + gb];   // earlier tokens of the block's list
+    qbase[gb] = p.offsets[h * nb + gb] + before;
+    pbase[gb] = p.wtile_off[sub_row + gb] * kTileRows + (before - p.chunk_hist[lo_row + gb]) * p.g;
+  }
   __syncthreads();
-  const int t = tile * p.idx_tok + tid;
+  const int t0 = tile * p.idx_tok;
+  const int t = t0 + tid;
   const bool live = tid < p.idx_tok && t < p.n;
   int32_t kgb[TP];
 #pragma unroll
@@ -360,37 +407,62 @@ __global__ void __launch_bounds__(kIdxThreads) scatter_kernel(Params p) {
   if (live && nb > 0) {
     bool bad = false;   // raised by the count pass already
     token_blocks<TP>(p, nb, h, t, kgb, bad);
+  }
+  {
+    const bool on = live && nb > 0;
+    const uint32_t act = __ballot_sync(0xffffffffu, on);
+    if (on) {
+      const int leader = __ffs(act) - 1;
+      uint32_t *mrow = masks + (tid >> 5) * nb;
 #pragma unroll
-    for (int k = 0; k < TP; ++k)
-      if (kgb[k] >= 0) atomicOr(&masks[(tid >> 5) * nb + kgb[k]], 1u << (tid & 31));
+      for (int k = 0; k < TP; ++k) {
+        const int32_t lead_gb = __shfl_sync(act, kgb[k], leader);
+        const uint32_t same = __ballot_sync(act, kgb[k] == lead_gb && kgb[k] >= 0);
+        if (kgb[k] >= 0) {
+          if (kgb[k] != lead_gb) atomicOr(&mrow[kgb[k]], 1u << lane);
+          else if (lane == leader) atomicOr(&mrow[kgb[k]], same);
+        }
+      }
+    }
   }
   __syncthreads();
-  if (!live) return;
-  const int wl = tid >> 5;
-  const uint32_t below = (1u << (tid & 31)) - 1u;
-  const int64_t hist_row = ((int64_t)h * p.n_idx_tiles + tile) * p.nb_max;
-  const int w = tile / p.wave_tiles;
-  const int64_t lo_row = ((int64_t)h * p.n_idx_tiles + (int64_t)w * p.wave_tiles) * p.nb_max;
-  int32_t *slot = p.slot_map + ((int64_t)h * p.n + t) * p.topk;
-  int32_t *prow = p.prow + ((int64_t)h * p.n + t) * p.topk;
-#pragma unroll
-  for (int k = 0; k < TP; ++k) {
-    if (k >= p.topk) break;
-    const int gb = kgb[k];
-    if (gb < 0) {
-      slot[k] = -1;
-      prow[k] = -1;
-      continue;
+  // tokens of earlier warps per (warp, block)
+  for (int gb = tid; gb < nb; gb += blockDim.x) {
+    int run = 0;
+    for (int w2 = 0; w2 < mw; ++w2) {
+      wpre[w2 * nb + gb] = static_cast<uint8_t>(run);
+      run += __popc(masks[w2 * nb + gb]);
     }
-    int32_t r = __popc(masks[wl * nb + gb] & below);
-    for (int w2 = 0; w2 < wl; ++w2) r += __popc(masks[w2 * nb + gb]);
-    const int32_t rank = p.chunk_hist[hist_row + gb] + r;   // rank inside block gb's list
-    const int32_t pos = p.offsets[h * nb + gb] + rank;
-    p.q_list[pos] = t;
-    slot[k] = pos;
-    const int32_t lo = p.chunk_hist[lo_row + gb];
-    const int64_t sub = ((int64_t)h * p.n_w + w) * p.nb_max + gb;
-    prow[k] = p.wtile_off[sub] * kTileRows + (rank - lo) * p.g;
+  }
+  __syncthreads();
+  const int ntok = min(p.idx_tok, p.n - t0);
+  if (live) {
+    const int wl = tid >> 5;
+    const uint32_t below = (1u << lane) - 1u;
+    int32_t *srow_t = srow + tid * p.topk;
+    int32_t *prow_t = prow_s + tid * p.topk;
+#pragma unroll
+    for (int k = 0; k < TP; ++k) {
+      if (k >= p.topk) break;
+      const int gb = kgb[k];
+      if (gb < 0) {
+        srow_t[k] = -1;
+        prow_t[k] = -1;
+        continue;
+      }
+      const int32_t r = __popc(masks[wl * nb + gb] & below) + wpre[wl * nb + gb];
+      const int32_t pos = qbase[gb] + r;
+      p.q_list[pos] = t;
+      srow_t[k] = pos;
+      prow_t[k] = pbase[gb] + r * p.g;
+    }
+  }
+  __syncthreads();
+  // the tile's rows of slot_map and prow are contiguous: coalesced copies
+  const int64_t base = ((int64_t)h * p.n + t0) * p.topk;
+  for (int i = tid; i < ntok * p.topk; i += blockDim.x) {
+    p.slot_map[base + i] = srow[i];
+    p.prow[base + i] = prow_s[i];
   }
 }
 
@@ -417,7 +489,7 @@ static void count_or_scatter(const Params &p, bool scatter, dim3 grid, size_t sm
 }
 
 size_t index_count_smem(const Params &p) { return sizeof(int32_t) * p.nb_max; }
-size_t index_scatter_smem(const Params &p) { return sizeof(uint32_t) * (p.idx_tok / 32) * p.nb_max; }
+size_t index_scatter_smem(const Params &p);
 
 cudaError_t launch_index(const Params &p, cudaStream_t stream, void (*mark)(int, cudaStream_t, bool)) {
   mark(0, stream, true);
@@ -428,14 +500,14 @@ cudaError_t launch_index(const Params &p, cudaStream_t stream, void (*mark)(int,
   count_or_scatter(p, false, grid_t, index_count_smem(p), stream);
   mark(1, stream, false);
   mark(2, stream, true);
-  col_scan_kernel<<<dim3(static_cast<unsigned>((p.nb_max + 31) / 32), p.h_k), dim3(32, 8), 0,
+  col_scan_kernel<<<dim3(static_cast<unsigned>((p.nb_max + 31) / 32), p.h_k), dim3(32, 32), 0,
                     stream>>>(p);
   mark(2, stream, false);
   mark(3, stream, true);
   scan_kernel<<<1, 1024, 0, stream>>>(p);
   wave_scan_local_kernel<<<static_cast<unsigned>(p.n_scan_ctas), 1024, 0, stream>>>(p);
   wave_scan_add_kernel<<<static_cast<unsigned>(p.n_scan_ctas), 1024, 0, stream>>>(p);
-  tile_desc_kernel<<<static_cast<unsigned>((p.nsub + 255) / 256), 256, 0, stream>>>(p);
+  tile_desc_kernel<<<static_cast<unsigned>((p.nsub + 7) / 8), 256, 0, stream>>>(p);
   mark(3, stream, false);
   mark(4, stream, true);
   count_or_scatter(p, true, grid_t, index_scatter_smem(p), stream);
