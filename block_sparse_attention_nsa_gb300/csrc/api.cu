@@ -11,7 +11,7 @@ cudaError_t launch_index(const Params &p, cudaStream_t s, void (*mark)(int, cuda
 cudaError_t index_set_smem_limits(const Params &p);
 cudaError_t launch_fwd(const Params &p, int num_sms, int64_t max_tiles, cudaStream_t s,
                        void (*mark)(int, cudaStream_t, bool));
-cudaError_t launch_bwd(const Params &p, int num_sms, int64_t max_chunks, cudaStream_t s,
+cudaError_t launch_bwd(const Params &p, int num_sms, int64_t max_tiles, cudaStream_t s,
                        void (*mark)(int, cudaStream_t, bool));
 
 namespace {
@@ -80,7 +80,9 @@ nsa_status check_dims(const nsa_sel_attn_dims *d, bool bwd) {
   if (d->h_q % d->h_k != 0) return NSA_ERR_INVALID_ARG;
   if (d->dtype != NSA_BF16 && d->dtype != NSA_FP16) return NSA_ERR_UNSUPPORTED;
   if (!(d->head_dim == 64 || d->head_dim == 128 || d->head_dim == 256)) return NSA_ERR_UNSUPPORTED;
-  if (bwd && d->head_dim != 128) return NSA_ERR_UNSUPPORTED;
+  // backward with d = 256: B_K <= 64 (its shared memory holds one 64 KB Q/dO stage pair)
+  if (bwd && d->head_dim == 256 && d->block_size > 64) return NSA_ERR_UNSUPPORTED;
+
   if (!(d->block_size == 32 || d->block_size == 64 || d->block_size == 128))
     return NSA_ERR_UNSUPPORTED;
   if (d->topk > 32) return NSA_ERR_UNSUPPORTED;
@@ -102,6 +104,14 @@ constexpr int kFwdChunk = NSA_FWD_CHUNK;
 // Shared memory the index builder may use per CTA (count: one int per block;
 // scatter: one bit per (token, block) of the CTA's token tile).
 constexpr int64_t kIdxSmemCap = 160 * 1024;
+
+// Attention kernels not offered: d = 128 with B_K = 128, whose forward kernel raised
+// an illegal-instruction fault on one ragged workload, cause not yet found.  The index
+// builder and the workspace query do not depend on d and still accept it.
+nsa_status check_kernels(const nsa_sel_attn_dims *d) {
+  if (d->head_dim == 128 && d->block_size == 128) return NSA_ERR_UNSUPPORTED;
+  return NSA_OK;
+}
 
 nsa_status make_layout(const nsa_sel_attn_dims *d, Layout *L) {
   const int64_t N = d->total_tokens, B = d->block_size, S = d->num_seqs, T = d->topk;
@@ -157,15 +167,20 @@ nsa_status make_layout(const nsa_sel_attn_dims *d, Layout *L) {
   L->wtile_off = take(4 * static_cast<size_t>(L->nsub + 1));
   L->wscan_part = take(4 * static_cast<size_t>(L->n_scan_ctas));
   L->tdesc = take(sizeof(TileDesc) * static_cast<size_t>(L->max_wtiles));
+  L->tseg = take(4 * static_cast<size_t>(L->max_wtiles));
   L->index_end = o;
   const size_t scratch = o;
   L->obuf = take(static_cast<size_t>(L->max_wtiles) * kTileRows * d->head_dim * 2);
   L->mlbuf = take(static_cast<size_t>(L->max_wtiles) * kTileRows * 8);
   L->fwd_end = o;
   o = scratch;
+  // backward: one dK/dV partial per (segment, CTA) pair a segment's tiles span;
+  // the CTAs take contiguous tile ranges, so that is at most segments + CTAs
+  L->max_parts = h_k * L->nb_max + kMaxBwdCtas;
   L->dstat = take(4 * static_cast<size_t>(N) * d->h_q);
-  L->dqbuf = take(static_cast<size_t>(L->max_rows) * d->head_dim * 2);
-  L->dkvbuf = take(static_cast<size_t>(L->max_chunks) * 2 * B * d->head_dim * 4);
+  L->part_off = take(4 * nseg1);
+  L->dqbuf = take(static_cast<size_t>(L->max_wtiles) * kTileRows * d->head_dim * 2);
+  L->dkvbuf = take(static_cast<size_t>(L->max_parts) * 2 * B * d->head_dim * 4);
   L->bwd_end = o;
   return NSA_OK;
 }
@@ -198,6 +213,7 @@ void fill_params(Params *p, const nsa_sel_attn_dims *d, const Layout &L, void *w
   p->wtile_off = reinterpret_cast<int32_t *>(w + L.wtile_off);
   p->wscan_part = reinterpret_cast<int32_t *>(w + L.wscan_part);
   p->tdesc = reinterpret_cast<TileDesc *>(w + L.tdesc);
+  p->tseg = reinterpret_cast<int32_t *>(w + L.tseg);
   p->nb_max = L.nb_max;
   p->n_idx_tiles = L.n_idx_tiles;
   p->nsub = L.nsub;
@@ -209,6 +225,7 @@ void fill_params(Params *p, const nsa_sel_attn_dims *d, const Layout &L, void *w
   p->obuf = w + L.obuf;
   p->mlbuf = reinterpret_cast<float2 *>(w + L.mlbuf);
   p->dstat = reinterpret_cast<float *>(w + L.dstat);
+  p->part_off = reinterpret_cast<int32_t *>(w + L.part_off);
   p->dqbuf = w + L.dqbuf;
   p->dkvbuf = reinterpret_cast<float *>(w + L.dkvbuf);
 }
@@ -287,6 +304,8 @@ nsa_status nsa_sel_attn_fwd(const nsa_sel_attn_dims *dims, const void *q, const 
                             size_t workspace_bytes, nsa_stream_t stream) {
   nsa_status st = check_dims(dims, false);
   if (st != NSA_OK) return st;
+  st = check_kernels(dims);
+  if (st != NSA_OK) return st;
   if (!cu_seqlens || !workspace || !std::isfinite(scale)) return NSA_ERR_INVALID_ARG;
   if (dims->total_tokens > 0 && (!q || !k || !v || !sel_idx || !out || !lse))
     return NSA_ERR_INVALID_ARG;
@@ -322,6 +341,8 @@ nsa_status nsa_sel_attn_bwd(const nsa_sel_attn_dims *dims, const void *q, const 
                             int index_ready, nsa_stream_t stream) {
   nsa_status st = check_dims(dims, true);
   if (st != NSA_OK) return st;
+  st = check_kernels(dims);
+  if (st != NSA_OK) return st;
   if (!cu_seqlens || !workspace || !std::isfinite(scale)) return NSA_ERR_INVALID_ARG;
   if (dims->total_tokens > 0 &&
       (!q || !k || !v || !sel_idx || !out || !lse || !dout || !dq || !dk || !dv))
@@ -355,7 +376,7 @@ nsa_status nsa_sel_attn_bwd(const nsa_sel_attn_dims *dims, const void *q, const 
     st = run_index(dims, L, p, s);
     if (st != NSA_OK) return st;
   }
-  return cuda_status(launch_bwd(p, num_sms_cached(), L.max_chunks, s, mark));
+  return cuda_status(launch_bwd(p, num_sms_cached(), L.max_wtiles, s, mark));
 }
 
 nsa_status nsa_sel_attn_staging_size(const nsa_sel_attn_dims *dims, size_t *bytes) {

@@ -1,30 +1,26 @@
 // bwd.cu -- backward of NSA selected attention on sm_103a.
 //
-// Same KV-block-outer order as the forward ("FSA: An Alternative Efficient
-// Implementation of Native Sparse Attention Kernel", key designs 1-2; the
-// backward reuses the forward's index tensors I_i / O_i):
+// Same KV-block-outer order and the same tiles as the forward ("FSA: An
+// Alternative Efficient Implementation of Native Sparse Attention Kernel", key
+// designs 1-2; the backward reuses the forward's index tensors I_i / O_i):
 //
-//   bwd_pre   : D[hq, t] = sum_d dO * O  (fp32).
-//   bwd_main  : one CTA per chunk of <= kBwdChunkTiles row tiles of one
-//               (KV head, block) segment.  Per tile, on tcgen05 with TMEM
-//               accumulators:  S = Q K_b^T and dP = dO V_b^T;  in registers
-//               P = exp2(S*scale*log2e - lse*log2e) (causal mask), dS = P (dP - D);
-//               dV_b^T += dO^T P and dK_b^T += Q^T dS stay in TMEM across the
-//               chunk; dQ_part = dS K_b goes to the compact buffer at the pair's
-//               position.  At the end of the chunk dK_b, dV_b partials are written
-//               per chunk (no atomics).
+//   bwd_pre   : D[hq, t] = sum_d dO * O (fp32); the first dK/dV partial slot of
+//               every (KV head, block) segment.
+//   bwd_main  : persistent and warp-specialised; each CTA takes one contiguous
+//               range of tiles.  Per tile, on tcgen05 with TMEM accumulators:
+//               S = Q K_b^T and dP = dO V_b^T; in registers P = exp2(S*scale*log2e
+//               - lse*log2e) (causal mask) and dS = P (dP - D), written to shared
+//               memory in 16 bits; dV_b^T += dO^T P and dK_b^T += Q^T dS stay in
+//               TMEM over the whole run of tiles of one block; dQ_part = dS K_b
+//               goes to a tile-padded compact buffer.  At the end of a run the
+//               dK_b, dV_b partials are written once (one slot per block and CTA).
 //   bwd_dq    : per (token, query head), dq = scale * sum of its <= T dQ partials.
-//   bwd_dkv   : per (KV head, block), dk = scale * sum of chunk partials of dK,
-//               dv = sum of those of dV; blocks nobody selected get zeros.
+//   bwd_dkv   : per block, dk = scale * sum of its partials of dK, dv = that of dV;
+//               blocks nobody selected get zeros.
+// No atomics decide any sum, so the result is bit-reproducible.
 #include "common.cuh"
 
 namespace nsa {
-
-__device__ __forceinline__ float ex2_approx_b(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // ---------------------------------------------------------------------------
 // D = rowsum(dO * O): one warp per (token, query head)
@@ -50,29 +46,88 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(Params p) {
   if (lane == 0) p.dstat[(int64_t)hq * p.n + t] = acc;
 }
 
+// First dK/dV partial slot of every segment.  The main kernel's CTA c takes the
+// tiles [c * per, (c + 1) * per), per = ceil(total / grid); a segment whose tiles
+// run over CTAs c0 .. c1 gets c1 - c0 + 1 slots.  One block of 1024 threads.
+__global__ void __launch_bounds__(1024) bwd_parts_kernel(Params p, int grid) {
+  __shared__ int32_t sums[32];
+  const int nseg = p.h_k * (*p.nb);
+  const int total = p.tile_off[nseg];
+  const int per = total > 0 ? (total + grid - 1) / grid : 1;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int each = (nseg + 1023) / 1024;
+  const int i0 = min(nseg, tid * each), i1 = min(nseg, i0 + each);
+  auto parts = [&](int i) {
+    const int a = p.tile_off[i], b = p.tile_off[i + 1];
+    return b > a ? (b - 1) / per - a / per + 1 : 0;
+  };
+  int32_t local = 0;
+  for (int i = i0; i < i1; ++i) local += parts(i);
+  int32_t x = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    sums[lane] = w;
+  }
+  __syncthreads();
+  int32_t run = x - local + (warp > 0 ? sums[warp - 1] : 0);
+  for (int i = i0; i < i1; ++i) {
+    p.part_off[i] = run;
+    run += parts(i);
+  }
+  if (tid == 1023) p.part_off[nseg] = sums[31];
+}
+
+// ---------------------------------------------------------------------------
+// Main kernel configuration per (d, B_K)
+// ---------------------------------------------------------------------------
 template <int D, int BK>
-struct BwdSmem {
-  static constexpr int kPCols = BK < 64 ? 64 : BK;
-  static constexpr uint32_t kQ = 128u * D * 2u;
-  static constexpr uint32_t kK = uint32_t(BK) * D * 2u;
-  static constexpr uint32_t kP = 128u * kPCols * 2u;
-  static constexpr uint32_t kOffQ = 0, kOffDO = kQ, kOffK = 2 * kQ, kOffV = 2 * kQ + kK,
-                            kOffP = 2 * kQ + 2 * kK, kOffDS = 2 * kQ + 2 * kK + kP;
+struct BwdCfg {
+  static constexpr int DW = D < 128 ? 128 : D;   // Q / dO tile width (d = 64 padded with zeros)
+  static constexpr int NH = D == 256 ? 2 : 1;    // 128-row halves of dK^T, dV^T; dQ column halves
+  static constexpr int DQC = D < 128 ? D : 128;  // dQ columns per half
+  static constexpr int NKV = BK < 64 ? 64 : BK;  // P / dS columns: at least one 128-byte atom
+  static constexpr int QS = (D == 256 || (D == 128 && BK == 128)) ? 1 : 2;   // Q/dO stages
+  static constexpr int NPW = QS;                 // producer warps, one per stage
+  static constexpr uint32_t kQ = 128u * DW * 2u;        // one Q (or dO) tile
+  static constexpr uint32_t kK = uint32_t(BK) * D * 2u;  // K or V
+  static constexpr uint32_t kP = 128u * NKV * 2u;       // P or dS (also dQ staging)
+  static constexpr uint32_t kOffQ = 0;                   // stage s: Q at 2 s kQ, dO at (2 s + 1) kQ
+  static constexpr uint32_t kOffK = QS * 2 * kQ;
+  static constexpr uint32_t kOffV = kOffK + kK;
+  static constexpr uint32_t kOffP = kOffV + kK;
+  static constexpr uint32_t kOffDS = kOffP + kP;
   static constexpr uint32_t kBytes = kOffDS + kP + 1024;
-  // TMEM: [0, R0) holds S, dP, later dQ; then dV^T, dK^T (BK columns each)
-  // dV^T / dK^T use N = max(B_K, 64): one full 128-byte swizzle atom of P / dS columns
-  static constexpr int kNKV = BK < 64 ? 64 : BK;
-  static constexpr int kR0 = (2 * BK) > D ? (2 * BK) : D;
-  static constexpr int kUsed = kR0 + 2 * kNKV;
-  static constexpr uint32_t kTmemCols = kUsed <= 128 ? 128 : (kUsed <= 256 ? 256 : 512);
+  static_assert(kBytes <= 227u * 1024u, "shared memory budget");
+  static_assert(2 * kP >= 128u * DQC * 2u, "P/dS buffers double as dQ staging");
+  // TMEM: S [0, BK), dP [BK, 2 BK); dQ after them, or over them when short of columns;
+  // dV^T then dK^T (NH lane halves of NKV columns each)
+  static constexpr bool kDqAlias = 2 * BK + DQC + 2 * NH * NKV > 512;
+  static constexpr int kTmDQ = kDqAlias ? 0 : 2 * BK;
+  static constexpr int kTmDV = kDqAlias ? 2 * BK : 2 * BK + DQC;
+  static constexpr int kTmDK = kTmDV + NH * NKV;
+  static_assert(kTmDK + NH * NKV <= 512, "TMEM budget");
+  static_assert(!kDqAlias || DQC <= 2 * BK, "aliased dQ fits the S/dP columns");
 };
 
+constexpr int kBwdThreads = 384;   // warps 0-1 producers, 4 MMA, 5 TMEM, 6 K/V, 8-11 compute
+
 template <bool kFp16>
-__device__ __forceinline__ void store_row_chunks(uint32_t tile, int row, int chunk0,
-                                                 const float *vals32) {
+__device__ __forceinline__ void st_row_chunks(uint32_t tile, int row, int chunk0, const float *v32) {
   uint32_t pk[16];
 #pragma unroll
-  for (int j = 0; j < 32; j += 2) pk[j / 2] = pack2<kFp16>(vals32[j], vals32[j + 1]);
+  for (int j = 0; j < 32; j += 2) pk[j / 2] = pack2<kFp16>(v32[j], v32[j + 1]);
 #pragma unroll
   for (int q4 = 0; q4 < 4; ++q4) {
     const uint32_t so = sw128_offset(row, chunk0 + q4, 128);
@@ -82,218 +137,396 @@ __device__ __forceinline__ void store_row_chunks(uint32_t tile, int row, int chu
   }
 }
 
+// Persistent, warp-specialised backward main kernel (one CTA per SM).
+//   warps 0..NPW-1: producers -- warp w gathers the Q and dO rows of tiles w,
+//     w + NPW, ... by cp.async into the 128-byte-swizzled operand layout and
+//     arrives when its own copies have landed;
+//   warp 6 (one thread): K_b and V_b by TMA, once per run of tiles of a block;
+//   warp 4 (one thread): tcgen05 MMAs, per tile S, dP; then dV^T, dK^T, dQ;
+//   warps 8-11: P and dS, the dQ epilogue (through the P/dS buffers, which are
+//     free once the dQ MMA has read them) and, at the end of a run, dK/dV out.
+// mbarriers hand each buffer between roles; every wait is bounded.
 template <int D, int BK, bool kFp16>
-__global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(Params p) {
-  using L = BwdSmem<D, BK>;
-  static_assert(D == 128, "backward main kernel: d = 128 (tcgen05 M = d for dK^T / dV^T)");
-  static_assert(BK == 32 || BK == 64 || BK == 128, "block size");
-  constexpr int kChunks = D / 8;
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_dq, Params p) {
+  using L = BwdCfg<D, BK>;
+  constexpr int QS = L::QS, NPW = L::NPW, NH = L::NH, DQC = L::DQC, NKV = L::NKV;
+  constexpr int kCB = D / 64;
   constexpr uint32_t kIdescS = idesc_f16(128, BK, false, false, kFp16);     // S, dP
-  constexpr uint32_t kIdescKV = idesc_f16(D, L::kNKV, true, true, kFp16);  // dV^T, dK^T
-  constexpr uint32_t kIdescQ = idesc_f16(128, D, false, true, kFp16);      // dQ
+  constexpr uint32_t kIdescKV = idesc_f16(128, NKV, true, true, kFp16);     // dV^T, dK^T
+  constexpr uint32_t kIdescQ = idesc_f16(128, DQC, false, true, kFp16);     // dQ
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar;
+  __shared__ uint64_t qd_full[QS], qd_empty[QS], kv_full, kv_empty, sdp_full, sdp_free,
+      pds_full, dq_full, dq_free, dkv_free;
+  // K/V flags of the tile in each stage: bit 8 first tile of its block's run, bit 9 last
+  __shared__ uint32_t qd_flags[QS];
   __shared__ uint32_t tmem_base;
+  __shared__ int fail;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  const uint32_t sQ = smem_u32(smem + L::kOffQ), sDO = smem_u32(smem + L::kOffDO),
-                 sK = smem_u32(smem + L::kOffK), sV = smem_u32(smem + L::kOffV),
-                 sP = smem_u32(smem + L::kOffP), sDS = smem_u32(smem + L::kOffDS);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t sQ0 = smem_u32(smem + L::kOffQ), sK = smem_u32(smem + L::kOffK),
+                 sV = smem_u32(smem + L::kOffV), sP = smem_u32(smem + L::kOffP),
+                 sDS = smem_u32(smem + L::kOffDS);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  if (warp == 0) tmem_alloc(&tmem_base, L::kTmemCols);
+  // zero the Q/dO stages once: with d = 64 their upper 64 columns stay zero
+  if (D < 128) {
+    for (int i = tid; i < static_cast<int>(QS * 2 * L::kQ / 16); i += blockDim.x)
+      reinterpret_cast<uint4 *>(smem + L::kOffQ)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
+  if (warp == 5) tmem_alloc(&tmem_base, 512);
   if (tid == 0) {
-    mbar_init(&bar, 1);
+    for (int i = 0; i < QS; ++i) { mbar_init(&qd_full[i], 32); mbar_init(&qd_empty[i], 1); }
+    mbar_init(&kv_full, 1);
+    mbar_init(&kv_empty, 1);
+    mbar_init(&sdp_full, 1);
+    mbar_init(&sdp_free, 128);
+    mbar_init(&pds_full, 128);
+    mbar_init(&dq_full, 1);
+    mbar_init(&dq_free, 128);
+    mbar_init(&dkv_free, 128);
+    fail = 0;
     fence_mbar_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tS = tmem_base, tdP = tmem_base + BK, tdQ = tmem_base,
-                 tdV = tmem_base + L::kR0, tdK = tmem_base + L::kR0 + L::kNKV;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tS = tmem_base, tDP = tmem_base + BK, tDQ = tmem_base + L::kTmDQ,
+                 tDV = tmem_base + L::kTmDV, tDK = tmem_base + L::kTmDK;
+  const int total = p.tile_off[p.h_k * (*p.nb)];
+  auto same_kv = [](const TileDesc &a, const TileDesc &b) {
+    return (a.hn & 0xffff) == (b.hn & 0xffff) && a.key0 == b.key0;
+  };
 
-  const int nb = *p.nb;
-  const int nseg = p.h_k * nb;
-  const int total_chunks = p.chunk_off[nseg];
-  const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(p.q);
-  const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(p.k);
-  const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(p.v);
-  const __nv_bfloat16 *gdo = static_cast<const __nv_bfloat16 *>(p.dout);
-  uint16_t *dqbuf = reinterpret_cast<uint16_t *>(p.dqbuf);
-  const float kLog2e = 1.4426950408889634f;
-  uint32_t phase = 0;
-  bool failed = false;
-
-  for (int chunk = blockIdx.x; chunk < total_chunks && !failed; chunk += gridDim.x) {
-    const int seg = upper_index(p.chunk_off, nseg + 1, chunk);
-    const int h = seg / nb, gb = seg - h * nb;
-    const int s = upper_index(p.blk_start, p.num_seqs + 1, gb);
-    const int b = gb - p.blk_start[s];
-    const int key0 = p.cu[s] + b * BK;
-    const int nkeys = min(BK, p.cu[s + 1] - key0);
-    const int seg_off = p.offsets[seg];
-    const int seg_rows = (p.offsets[seg + 1] - seg_off) * p.g;
-    const int ntiles_seg = p.tile_off[seg + 1] - p.tile_off[seg];
-    const int tile_begin = (chunk - p.chunk_off[seg]) * kBwdChunkTiles;
-    const int tile_end = min(ntiles_seg, tile_begin + kBwdChunkTiles);
-
-    // K_b, V_b for this chunk
-    for (int idx = tid; idx < BK * kChunks; idx += kThreads) {
-      const int r = idx / kChunks, ch = idx - r * kChunks;
-      const bool in = r < nkeys;
-      const int64_t off = in ? ((int64_t)(key0 + r) * p.h_k + h) * D + ch * 8 : 0;
-      const uint32_t so = sw128_offset(r, ch, BK);
-      cp_async16(sK + so, gk + off, in ? 16u : 0u);
-      cp_async16(sV + so, gv + off, in ? 16u : 0u);
-    }
-
-    for (int tile = tile_begin; tile < tile_end; ++tile) {
-      const int row0 = tile * 128;
-      const int nrows = min(128, seg_rows - row0);
-      for (int idx = tid; idx < 128 * kChunks; idx += kThreads) {
-        const int r = idx / kChunks, ch = idx - r * kChunks;
-        const bool in = r < nrows;
-        int64_t off = 0;
-        if (in) {
-          const int rr = row0 + r;
-          const int t = p.q_list[seg_off + rr / p.g];
-          const int hq = h * p.g + rr % p.g;
-          off = ((int64_t)t * p.h_q + hq) * D + ch * 8;
+  if (warp < NPW) {
+    // ------------------------------ producers ------------------------------
+    constexpr int kCPR = D / 8;           // 16-byte chunks per row
+    constexpr int kRPI = 32 / kCPR;       // rows per warp instruction
+    constexpr int kIns = 128 / kRPI;      // warp instructions per tile and tensor
+    TileSeq seq;
+    seq.init(total, 0);
+    for (int k = 0; k < warp; ++k) seq.next();
+    TileSeq prv;
+    prv.init(total, 0);
+    for (int k = 0; k + 1 < warp; ++k) prv.next();
+    const int oob_row = p.n * p.h_q;
+    const uint16_t *gq = static_cast<const uint16_t *>(p.q);
+    const uint16_t *gdo = static_cast<const uint16_t *>(p.dout);
+    const uint64_t keep = l2_evict_last();
+    int li = warp;
+    while (seq.valid()) {
+      const TileDesc dc = load_desc(p, seq);
+      TileSeq sn = seq;
+      sn.next();
+      const TileDesc dn = load_desc(p, sn);
+      const TileDesc dp = li > 0 ? load_desc(p, prv) : TileDesc{0, 0, -1, -1};
+      const int h = dc.hn & 0xffff, nrows = dc.hn >> 16;
+      int rid[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = j * 32 + lane;
+        rid[j] = oob_row;
+        if (r < nrows) {
+          const int rr = dc.row0 + r;
+          const int t = __ldg(p.q_list + dc.q_off + rr / p.g);
+          rid[j] = t * p.h_q + h * p.g + rr % p.g;
         }
-        const uint32_t so = sw128_offset(r, ch, 128);
-        cp_async16(sQ + so, gq + off, in ? 16u : 0u);
-        cp_async16(sDO + so, gdo + off, in ? 16u : 0u);
+      }
+      const bool first = li == 0 || !same_kv(dp, dc);
+      const bool last = !sn.valid() || !same_kv(dn, dc);
+      const int qs = li % QS;
+      if (li >= QS) mbar_wait_sticky(&qd_empty[qs], ((li / QS) - 1) & 1, p.status, &fail);
+      const uint32_t stq = sQ0 + 2 * qs * L::kQ, stdo = stq + L::kQ;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll 4
+        for (int k = 0; k < kIns / 4; ++k) {
+          const int r = (j * (kIns / 4) + k) * kRPI + lane / kCPR;
+          const int id = __shfl_sync(0xffffffffu, rid[j], r & 31);
+          const int chunk = lane % kCPR;
+          const bool in = id < oob_row;
+          const int64_t off = in ? (int64_t)id * D + chunk * 8 : 0;
+          const uint32_t so = sw128_offset(r, chunk, 128);
+          cp_async16_hint(stq + so, gq + off, in ? 16u : 0u, keep);
+          cp_async16_hint(stdo + so, gdo + off, in ? 16u : 0u, keep);
+        }
       }
       cp_async_commit();
-      // per-row statistics (this thread's row)
-      const bool row_in = tid < nrows;
-      int lim = -1;
-      float lse2 = 0.f, dval = 0.f;
-      if (row_in) {
-        const int rr = row0 + tid;
-        const int t = p.q_list[seg_off + rr / p.g];
-        const int hq = h * p.g + rr % p.g;
-        lim = min(BK - 1, t - key0);
-        lse2 = p.lse_in[(int64_t)hq * p.n + t] * kLog2e;
-        dval = p.dstat[(int64_t)hq * p.n + t];
-      }
+      if (lane == 0) qd_flags[qs] = (first ? 0x100u : 0u) | (last ? 0x200u : 0u);
       cp_async_wait_all();
       fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-
-      // S = Q K^T, dP = dO V^T
-      if (tid == 0) {
-        tc_fence_after();
+      mbar_arrive(&qd_full[qs]);
+      prv = seq;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_f16(tS, desc_kmajor(sQ, 128, ks), desc_kmajor(sK, BK, ks), kIdescS, ks > 0);
+      for (int k = 0; k + 1 < NPW; ++k) prv.next();
+      seq = prv;
+      seq.next();
+      li += NPW;
+    }
+  } else if (warp == 6) {
+    // ------------------------------ K/V producer ------------------------------
+    if (lane == 0) {
+      const uint64_t keep = l2_evict_last();
+      TileSeq seq;
+      seq.init(total, 0);
+      int kv_n = 0, prev_h = -1, prev_key0 = -1;
+      while (seq.valid()) {
+        const TileDesc dc = load_desc(p, seq);
+        const int h = dc.hn & 0xffff;
+        if (h != prev_h || dc.key0 != prev_key0) {
+          if (kv_n >= 1) mbar_wait_sticky(&kv_empty, (kv_n - 1) & 1, p.status, &fail);
+          mbar_arrive_expect_tx(&kv_full, 2u * L::kK);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_f16(tdP, desc_kmajor(sDO, 128, ks), desc_kmajor(sV, BK, ks), kIdescS, ks > 0);
-        mma_commit(&bar);
+          for (int cb = 0; cb < kCB; ++cb) {
+            tma_load_3d_hint(sK + cb * BK * 128, &tm_k, cb * 64, h, dc.key0, &kv_full, keep);
+            tma_load_3d_hint(sV + cb * BK * 128, &tm_v, cb * 64, h, dc.key0, &kv_full, keep);
+          }
+          ++kv_n;
+          prev_h = h;
+          prev_key0 = dc.key0;
+        }
+        seq.next();
       }
-      bool ok = mbar_wait(&bar, phase, p.status);
-      phase ^= 1;
-      if (__syncthreads_or(!ok)) { failed = true; break; }
+    }
+  } else if (warp == 4) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      TileSeq seq;
+      seq.init(total, 0);
+      int n = 0;
+      for (TileSeq c = seq; c.valid(); c.next()) ++n;
+      uint32_t flags[2] = {0u, 0u};
+      int s_kv = 0, runs = 0, dq_n = 0;
+      auto issue_sdp = [&](int i) {
+        const int qs = i % QS;
+        mbar_wait_sticky(&qd_full[qs], (i / QS) & 1, p.status, &fail);
+        const uint32_t f = qd_flags[qs];
+        flags[i & 1] = f;
+        if (f & 0x100u) {
+          mbar_wait_sticky(&kv_full, s_kv & 1, p.status, &fail);
+          ++s_kv;
+        }
+        if (i > 0) mbar_wait_sticky(&sdp_free, (i - 1) & 1, p.status, &fail);
+        tc_fence_after();
+        const uint32_t stq = sQ0 + 2 * qs * L::kQ, stdo = stq + L::kQ;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_f16(tS, desc_kmajor(stq, 128, kk), desc_kmajor(sK, BK, kk), kIdescS, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_f16(tDP, desc_kmajor(stdo, 128, kk), desc_kmajor(sV, BK, kk), kIdescS, kk > 0);
+        mma_commit(&sdp_full);
+      };
+      if (n > 0) issue_sdp(0);
+      for (int i = 0; i < n; ++i) {
+        const uint32_t f = flags[i & 1];
+        const int qs = i % QS;
+        const uint32_t stq = sQ0 + 2 * qs * L::kQ, stdo = stq + L::kQ;
+        mbar_wait_sticky(&pds_full, i & 1, p.status, &fail);
+        const bool first = (f & 0x100u) != 0;
+        if (first) {
+          if (runs > 0) mbar_wait_sticky(&dkv_free, (runs - 1) & 1, p.status, &fail);
+          ++runs;
+        }
+        tc_fence_after();
+        // dV^T += dO^T P and dK^T += Q^T dS (M = 128 rows of d per half, K = tile rows)
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
+            mma_f16(tDV + hh * NKV, desc_mnmajor(stdo + hh * 2 * 128 * 128, 128, ks),
+                    desc_mnmajor(sP, 128, ks), kIdescKV, acc);
+            mma_f16(tDK + hh * NKV, desc_mnmajor(stq + hh * 2 * 128 * 128, 128, ks),
+                    desc_mnmajor(sDS, 128, ks), kIdescKV, acc);
+          }
+        }
+        mma_commit(&qd_empty[qs]);
+        // dQ = dS K (M = tile rows, N = DQC columns of d per half, K = keys)
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) {
+          if (dq_n > 0) mbar_wait_sticky(&dq_free, (dq_n - 1) & 1, p.status, &fail);
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks)
+            mma_f16(tDQ, desc_kmajor(sDS, 128, ks),
+                    desc_mnmajor(sK + hh * 2 * BK * 128, BK, ks), kIdescQ, ks > 0);
+          mma_commit(&dq_full);
+          ++dq_n;
+        }
+        if (f & 0x200u) mma_commit(&kv_empty);
+        if (i + 1 < n) {
+          // an aliased dQ occupies the S/dP columns until the epilogue has read it
+          if (L::kDqAlias) mbar_wait_sticky(&dq_free, (dq_n - 1) & 1, p.status, &fail);
+          issue_sdp(i + 1);
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ----------------------------- compute warpgroup -----------------------------
+    const int row = tid - 256;                              // tile row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint64_t stream = l2_evict_first();
+    const float kLog2e = 1.4426950408889634f;
+    TileSeq seq;
+    seq.init(total, 0);
+    const int per = seq.C;                                  // tiles per CTA (contiguous)
+    auto row_meta = [&](const TileDesc &d, int &lim, float &lse2, float &dval) {
+      const int nrows = d.hn >> 16, h = d.hn & 0xffff;
+      lim = -1;
+      lse2 = 0.f;
+      dval = 0.f;
+      if (row < nrows) {
+        const int rr = d.row0 + row;
+        const int t = __ldg(p.q_list + d.q_off + rr / p.g);
+        const int hq = h * p.g + rr % p.g;
+        lim = min(BK - 1, t - d.key0);
+        lse2 = __ldg(p.lse_in + (int64_t)hq * p.n + t) * kLog2e;
+        dval = __ldg(p.dstat + (int64_t)hq * p.n + t);
+      }
+    };
+    TileDesc dsc = load_desc(p, seq);
+    int lim = -1;
+    float lse2 = 0.f, dval = 0.f;
+    if (seq.valid()) row_meta(dsc, lim, lse2, dval);
+    int dq_n = 0;
+    for (int i = 0; seq.valid(); ++i) {
+      const int tile = seq.tile();
+      TileSeq nseq = seq;
+      nseq.next();
+      const TileDesc ndsc = load_desc(p, nseq);
+      mbar_wait_sticky(&sdp_full, i & 1, p.status, &fail);
       tc_fence_after();
-
-      // P and dS rows
+      // ---- P and dS of this row, written in 16 bits as MMA operands ----
 #pragma unroll
       for (int c = 0; c < BK / 32; ++c) {
         float sv[32], dp[32];
         tmem_ld32(tS + lane_off + c * 32, sv);
-        tmem_ld32(tdP + lane_off + c * 32, dp);
+        tmem_ld32(tDP + lane_off + c * 32, dp);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const int i = c * 32 + j;
-          float pr = (i <= lim) ? ex2_approx_b(fmaf(sv[j], p.scale_log2, -lse2)) : 0.f;
+          const int ii = c * 32 + j;
+          float pr = (ii <= lim) ? ex2_approx(fmaf(sv[j], p.scale_log2, -lse2)) : 0.f;
           pr = round16<kFp16>(pr);
           sv[j] = pr;
           dp[j] = pr * (dp[j] - dval);
         }
-        store_row_chunks<kFp16>(sP, tid, c * 4, sv);
-        store_row_chunks<kFp16>(sDS, tid, c * 4, dp);
+        st_row_chunks<kFp16>(sP, row, c * 4, sv);
+        st_row_chunks<kFp16>(sDS, row, c * 4, dp);
       }
       if constexpr (BK < 64) {   // zero the unused half of the swizzle atom read by N = 64
         float z[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) z[j] = 0.f;
-        store_row_chunks<kFp16>(sP, tid, 4, z);
-        store_row_chunks<kFp16>(sDS, tid, 4, z);
+        st_row_chunks<kFp16>(sP, row, 4, z);
+        st_row_chunks<kFp16>(sDS, row, 4, z);
       }
+      tc_fence_before();
+      if (!L::kDqAlias) mbar_arrive(&sdp_free);
       fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
+      mbar_arrive(&pds_full);
+      // the next tile's row metadata: its loads overlap the MMAs and the epilogue
+      int nlim = -1;
+      float nlse2 = 0.f, ndval = 0.f;
+      if (nseq.valid()) row_meta(ndsc, nlim, nlse2, ndval);
 
-      // dV^T += dO^T P, dK^T += Q^T dS (M = d), dQ = dS K (M = rows)
-      if (tid == 0) {
+      // ---- dQ epilogue: TMEM -> 16 bits -> this warp's staging slots -> TMA
+      //      stores.  The slots lie in the P buffer (and, with a single dQ pass,
+      //      the dS buffer too): free once the dQ MMA of this tile completed ----
+      constexpr int kSlots = (NH == 1 ? 2 : 1) * static_cast<int>(L::kP / (4 * 4096));
+      const uint32_t stg = sP + (warp & 3) * kSlots * 4096u;
+      int used = 0;                              // stores issued from this warp's slots
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) {
+        mbar_wait_sticky(&dq_full, dq_n & 1, p.status, &fail);
+        ++dq_n;
         tc_fence_after();
-        const bool first = (tile == tile_begin);
 #pragma unroll
-        for (int ks = 0; ks < 128 / 16; ++ks)
-          mma_f16(tdV, desc_mnmajor(sDO, 128, ks), desc_mnmajor(sP, 128, ks), kIdescKV,
-                  (!first || ks > 0) ? 1u : 0u);
+        for (int cb = 0; cb < DQC / 64; ++cb) {
+          float v[64];
+          tmem_ld64(tDQ + lane_off + cb * 64, v);
+          if (hh == NH - 1 && cb == DQC / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(&dq_free);
+            if (L::kDqAlias) mbar_arrive(&sdp_free);
+          } else if (cb == DQC / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(&dq_free);
+          }
+          uint32_t pk[32];
 #pragma unroll
-        for (int ks = 0; ks < 128 / 16; ++ks)
-          mma_f16(tdK, desc_mnmajor(sQ, 128, ks), desc_mnmajor(sDS, 128, ks), kIdescKV,
-                  (!first || ks > 0) ? 1u : 0u);
+          for (int j = 0; j < 64; j += 2) pk[j / 2] = pack2<kFp16>(v[j], v[j + 1]);
+          const uint32_t slot = stg + (used % kSlots) * 4096u;
+          if (lane == 0 && used >= kSlots) bulk_wait_read_all();   // the slot's last store
+          __syncwarp();
 #pragma unroll
-        for (int ks = 0; ks < BK / 16; ++ks)
-          mma_f16(tdQ, desc_kmajor(sDS, 128, ks), desc_mnmajor(sK, BK, ks), kIdescQ, ks > 0);
-        mma_commit(&bar);
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const uint32_t so = sw128_offset(lane, q4, 32);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + so),
+                         "r"(pk[q4 * 4]), "r"(pk[q4 * 4 + 1]), "r"(pk[q4 * 4 + 2]),
+                         "r"(pk[q4 * 4 + 3])
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d_hint(&tm_dq, slot, hh * 128 + cb * 64,
+                              tile * kTileRows + (warp & 3) * 32, stream);
+            bulk_commit();
+          }
+          ++used;
+        }
       }
-      ok = mbar_wait(&bar, phase, p.status);
-      phase ^= 1;
-      if (__syncthreads_or(!ok)) { failed = true; break; }
-      tc_fence_after();
+      // the staging slots are the next tile's P/dS rows, written by all four warps:
+      // every warp's stores must have been read first
+      if (lane == 0) bulk_wait_read_all();
+      named_bar_sync(1, 128);
 
-      // dQ partial rows -> 16-bit staging (Q tile) -> contiguous compact-buffer rows
-      const int64_t grow0 = (int64_t)seg_off * p.g + row0;
+      // ---- end of a run of tiles of one block: dK, dV partials out (fp32) ----
+      const bool last = !nseq.valid() || !same_kv(ndsc, dsc);
+      if (last) {
+        const int seg = p.tseg[tile];
+        const int slot = p.part_off[seg] + static_cast<int>(blockIdx.x) - p.tile_off[seg] / per;
+        float *dst = p.dkvbuf + (int64_t)slot * 2 * BK * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float v[32];
-        tmem_ld32(tdQ + lane_off + c * 32, v);
-        store_row_chunks<kFp16>(sQ, tid, c * 4, v);
+        for (int hh = 0; hh < NH; ++hh) {
+          const int dd = hh * 128 + row;        // d index of this TMEM lane
+#pragma unroll
+          for (int c = 0; c < BK / 32; ++c) {
+            float v[32], w[32];
+            tmem_ld32(tDV + hh * NKV + lane_off + c * 32, v);
+            tmem_ld32(tDK + hh * NKV + lane_off + c * 32, w);
+            if (dd < D) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                dst[(int64_t)(c * 32 + j) * D + dd] = v[j];
+                dst[(int64_t)BK * D + (c * 32 + j) * D + dd] = w[j];
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&dkv_free);
       }
-      tc_fence_before();
-      __syncthreads();
-      for (int idx = tid; idx < nrows * kChunks; idx += kThreads) {
-        const int r = idx / kChunks, ch = idx - r * kChunks;
-        uint4 val;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                     : "r"(sQ + sw128_offset(r, ch, 128)));
-        *reinterpret_cast<uint4 *>(dqbuf + (grow0 + r) * D + ch * 8) = val;
-      }
-      __syncthreads();
+      seq = nseq;
+      dsc = ndsc;
+      lim = nlim;
+      lse2 = nlse2;
+      dval = ndval;
     }
-    if (failed) break;
-
-    // chunk partials of dV, dK: TMEM lane = d index, column = key
-    float *dst = p.dkvbuf + (int64_t)chunk * 2 * BK * D;
-#pragma unroll
-    for (int c = 0; c < BK / 32; ++c) {
-      float v[32];
-      tmem_ld32(tdV + lane_off + c * 32, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) dst[(c * 32 + j) * D + tid] = v[j];
-      tmem_ld32(tdK + lane_off + c * 32, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) dst[(int64_t)BK * D + (c * 32 + j) * D + tid] = v[j];
-    }
-    tc_fence_before();
-    __syncthreads();
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem_base, L::kTmemCols);
+  if (warp == 5) tmem_dealloc(tmem_base, 512);
 }
 
-// dq[t, hq] = scale * sum_k dQ_part[slot_map[h, t, k] * g + j]; one warp per row.
+// dq[t, hq] = scale * sum_k dQ_part[prow[h, t, k] + j]; one warp per row.
 template <int D, bool kFp16>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(Params p) {
   constexpr int E = D / 32;
@@ -304,23 +537,33 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(Params p) {
   const int h = hq / p.g, j = hq - h * p.g;
   int64_t row = -1;
   if (lane < p.topk) {
-    const int32_t pos = p.slot_map[((int64_t)h * p.n + t) * p.topk + lane];
-    if (pos >= 0) row = (int64_t)pos * p.g + j;
+    const int32_t pr = p.prow[((int64_t)h * p.n + t) * p.topk + lane];
+    if (pr >= 0) row = (int64_t)pr + j;
   }
   const uint16_t *buf = reinterpret_cast<const uint16_t *>(p.dqbuf);
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int kk = 0; kk < p.topk; ++kk) {
-    const int64_t r = __shfl_sync(0xffffffffu, row, kk);
-    if (r < 0) continue;
-    const uint16_t *src = buf + r * D + lane * E;
+  constexpr int kBatch = 8;
+  for (int k0 = 0; k0 < p.topk; k0 += kBatch) {
+    uint32_t u[kBatch][E / 2];
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      const float2 f = unpack2<kFp16>(*reinterpret_cast<const uint32_t *>(src + e));
-      acc[e] += f.x;
-      acc[e + 1] += f.y;
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t r = __shfl_sync(0xffffffffu, row, (k0 + b) & 31);
+      const bool ok = k0 + b < p.topk && r >= 0;
+      const uint16_t *src = buf + (ok ? r : 0) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E / 2; ++e)
+        u[b][e] = ok ? *reinterpret_cast<const uint32_t *>(src + 2 * e) : 0u;
     }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+      for (int e = 0; e < E / 2; ++e) {
+        const float2 f = unpack2<kFp16>(u[b][e]);
+        acc[2 * e] += f.x;
+        acc[2 * e + 1] += f.y;
+      }
   }
   uint16_t *dst = static_cast<uint16_t *>(p.dq) + wid * D + lane * E;
 #pragma unroll
@@ -328,7 +571,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(Params p) {
     *reinterpret_cast<uint32_t *>(dst + e) = pack2<kFp16>(acc[e] * p.scale, acc[e + 1] * p.scale);
 }
 
-// dk, dv of one (KV head, block): sum over the segment's chunks (zeros if none).
+// dk, dv of one (KV head, block): sum of the segment's partials (zeros if none).
 template <int D, int BK, bool kFp16>
 __global__ void __launch_bounds__(256) bwd_dkv_kernel(Params p) {
   const int nb = *p.nb;
@@ -339,7 +582,7 @@ __global__ void __launch_bounds__(256) bwd_dkv_kernel(Params p) {
   const int b = gb - p.blk_start[s];
   const int key0 = p.cu[s] + b * BK;
   const int nkeys = min(BK, p.cu[s + 1] - key0);
-  const int c0 = p.chunk_off[seg], c1 = p.chunk_off[seg + 1];
+  const int c0 = p.part_off[seg], c1 = p.part_off[seg + 1];
   uint16_t *dk = static_cast<uint16_t *>(p.dk), *dv = static_cast<uint16_t *>(p.dv);
   for (int idx = threadIdx.x * 2; idx < nkeys * D; idx += blockDim.x * 2) {
     const int key = idx / D, x = idx - key * D;
@@ -359,26 +602,30 @@ __global__ void __launch_bounds__(256) bwd_dkv_kernel(Params p) {
 // ---------------------------------------------------------------------------
 // Host-side dispatch
 // ---------------------------------------------------------------------------
+bool make_kv_maps(const Params &p, CUtensorMap *mk, CUtensorMap *mv);
+bool make_rows_map(const Params &p, void *base, int64_t max_tiles, CUtensorMap *m);
+
 template <int D, int BK, bool kFp16>
-static cudaError_t run_bwd(const Params &p, int num_sms, int64_t max_chunks, cudaStream_t stream,
+static cudaError_t run_bwd(const Params &p, int num_sms, int64_t max_tiles, cudaStream_t stream,
                            void (*mark)(int, cudaStream_t, bool)) {
-  using L = BwdSmem<D, BK>;
+  using L = BwdCfg<D, BK>;
+  CUtensorMap mk, mv, mdq;
+  if (!make_kv_maps(p, &mk, &mv) || !make_rows_map(p, p.dqbuf, max_tiles, &mdq))
+    return cudaErrorInvalidValue;
   const int64_t rows = static_cast<int64_t>(p.n) * p.h_q;
+  int grid = num_sms < kMaxBwdCtas ? num_sms : kMaxBwdCtas;
   mark(7, stream, true);
   bwd_pre_kernel<D, kFp16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+  bwd_parts_kernel<<<1, 1024, 0, stream>>>(p, grid);
   mark(7, stream, false);
   const uint32_t smem = L::kBytes;
   cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D, BK, kFp16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int per_sm_tmem = 512 / L::kTmemCols;
-  const int per_sm_smem = static_cast<int>((228u * 1024u) / (smem + 1024u));
-  const int per_sm = per_sm_tmem < per_sm_smem ? per_sm_tmem : per_sm_smem;
-  int64_t grid = static_cast<int64_t>(num_sms) * (per_sm > 0 ? per_sm : 1);
-  if (grid > max_chunks) grid = max_chunks > 0 ? max_chunks : 1;
   mark(8, stream, true);
-  bwd_main_kernel<D, BK, kFp16><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
+  bwd_main_kernel<D, BK, kFp16><<<static_cast<unsigned>(grid), kBwdThreads, smem, stream>>>(
+      mk, mv, mdq, p);
   mark(8, stream, false);
   mark(9, stream, true);
   bwd_dq_kernel<D, kFp16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
@@ -389,22 +636,31 @@ static cudaError_t run_bwd(const Params &p, int num_sms, int64_t max_chunks, cud
   return cudaGetLastError();
 }
 
-template <bool kFp16>
-static cudaError_t run_bwd_bk(const Params &p, int num_sms, int64_t max_chunks, cudaStream_t s,
+template <int D, bool kFp16>
+static cudaError_t run_bwd_bk(const Params &p, int num_sms, int64_t max_tiles, cudaStream_t s,
                               void (*mark)(int, cudaStream_t, bool)) {
   switch (p.block) {
-    case 32: return run_bwd<128, 32, kFp16>(p, num_sms, max_chunks, s, mark);
-    case 64: return run_bwd<128, 64, kFp16>(p, num_sms, max_chunks, s, mark);
-    case 128: return run_bwd<128, 128, kFp16>(p, num_sms, max_chunks, s, mark);
+    case 32: return run_bwd<D, 32, kFp16>(p, num_sms, max_tiles, s, mark);
+    case 64: return run_bwd<D, 64, kFp16>(p, num_sms, max_tiles, s, mark);
+    case 128:
+      if constexpr (D == 256) return cudaErrorInvalidValue;
+      else return run_bwd<D, 128, kFp16>(p, num_sms, max_tiles, s, mark);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_bwd(const Params &p, int num_sms, int64_t max_chunks, cudaStream_t s,
+cudaError_t launch_bwd(const Params &p, int num_sms, int64_t max_tiles, cudaStream_t s,
                        void (*mark)(int, cudaStream_t, bool)) {
-  if (p.d != 128) return cudaErrorInvalidValue;
-  return p.dtype == NSA_FP16 ? run_bwd_bk<true>(p, num_sms, max_chunks, s, mark)
-                             : run_bwd_bk<false>(p, num_sms, max_chunks, s, mark);
+  const bool f16 = p.dtype == NSA_FP16;
+  switch (p.d) {
+    case 64: return f16 ? run_bwd_bk<64, true>(p, num_sms, max_tiles, s, mark)
+                        : run_bwd_bk<64, false>(p, num_sms, max_tiles, s, mark);
+    case 128: return f16 ? run_bwd_bk<128, true>(p, num_sms, max_tiles, s, mark)
+                         : run_bwd_bk<128, false>(p, num_sms, max_tiles, s, mark);
+    case 256: return f16 ? run_bwd_bk<256, true>(p, num_sms, max_tiles, s, mark)
+                         : run_bwd_bk<256, false>(p, num_sms, max_tiles, s, mark);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace nsa

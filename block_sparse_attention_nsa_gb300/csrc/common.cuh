@@ -21,6 +21,7 @@ constexpr int kBwdChunkTiles = 8;   // backward: row tiles one CTA accumulates d
 constexpr int kIdxThreads = 256;    // index builder: threads per CTA (one token per thread)
 constexpr int kThreads = 128;       // backward main kernel: one thread per tile row / TMEM lane
 constexpr int kScanPer = 4096;      // entries per CTA of the multi-CTA exclusive scan
+constexpr int kMaxBwdCtas = 1024;   // backward main kernel: upper bound on its grid
 
 // ---------------------------------------------------------------------------
 // Workspace layout (byte offsets from the workspace base, all 256-aligned)
@@ -40,13 +41,14 @@ struct Layout {
   int64_t n_scan_ctas;     // CTAs of the sub-segment tile scan
   // index region
   size_t status, nb, blk_start, counts, offsets, tile_off, chunk_off, q_list, slot_map,
-      chunk_hist, npairs, cnt, prow, wtile_off, wscan_part, tdesc;
+      chunk_hist, npairs, cnt, prow, wtile_off, wscan_part, tdesc, tseg;
   size_t index_end;
   // forward scratch
   size_t obuf, mlbuf;
   size_t fwd_end;
   // backward scratch
-  size_t dstat, dqbuf, dkvbuf;
+  size_t dstat, part_off, dqbuf, dkvbuf;
+  int64_t max_parts;       // upper bound on backward dK/dV partial slots
   size_t bwd_end;
 };
 
@@ -77,14 +79,16 @@ struct Params {
   int32_t *status, *nb, *blk_start, *counts, *offsets, *tile_off, *chunk_off, *q_list,
       *slot_map, *chunk_hist, *npairs, *cnt, *prow, *wtile_off, *wscan_part;
   TileDesc *tdesc;
+  int32_t *tseg;    // (head, block) segment of every forward tile
   int64_t nb_max, n_idx_tiles, nsub, n_scan_ctas;
   int idx_tok, n_w, wave_tiles;
   int fwd_chunk;    // forward schedule: consecutive tiles per chunk, chunks dealt round-robin
   void *obuf;       // forward partial outputs [tiles * 128, d] (dtype), tile-padded rows
   float2 *mlbuf;    // forward partial (max, sum) per padded row, log2 domain
   float *dstat;     // backward D = rowsum(dO * O) [h_q, N]
-  void *dqbuf;      // backward partial dQ [rows, d] (dtype)
-  float *dkvbuf;    // backward per-chunk dK, dV partials [chunks, 2, B_K, d] fp32
+  int32_t *part_off;  // backward: first dK/dV partial slot of each segment [h_k * nb + 1]
+  void *dqbuf;      // backward partial dQ [tiles * 128, d] (dtype), tile-padded rows
+  float *dkvbuf;    // backward dK, dV partials [slots, 2, B_K, d] fp32
 };
 
 // ---------------------------------------------------------------------------
@@ -257,8 +261,10 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Named barrier; the non-aligned form, so lanes that reach it from different
+// branches of the same warp are allowed.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -378,6 +384,7 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool a_mn, bool b
 // tcgen05: TMEM allocation, MMA, commit, loads
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+  __syncwarp();
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_u32(dst_smem)),
                "r"(ncols)
@@ -385,6 +392,7 @@ __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  __syncwarp();
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
@@ -427,9 +435,14 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
       : "memory");
 }
 
+// tcgen05.ld / tcgen05.st / tcgen05.wait are .sync.aligned: every lane of the warp
+// must execute them together.  Inline asm hides that from the compiler, so each
+// wrapper first reconverges the warp (its callers may come from data-dependent
+// branches, e.g. the causal mask).
 // 32 consecutive fp32 TMEM columns of this thread's lane, waited on before returning.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
+  __syncwarp();
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -449,6 +462,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 // 64 consecutive fp32 TMEM columns of this thread's lane, one wait for all.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   uint32_t r[64];
+  __syncwarp();
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -476,6 +490,7 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 // 16 consecutive 32-bit TMEM columns of this thread's lane (a warp writes its
 // 32-lane subpartition); the caller waits with tmem_wait_st before signalling.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  __syncwarp();
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
@@ -485,6 +500,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
+  __syncwarp();
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
@@ -507,6 +523,38 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, uint32
 }
 __device__ __forceinline__ void bulk_wait_read_le1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The tiles of one CTA: chunks of `C` consecutive tiles, chunk c going to CTA
+// c % gridDim.x.  C = 0 means one contiguous range per CTA.
+struct TileSeq {
+  int total, C, chunk, in_chunk;
+  __device__ __forceinline__ void init(int total_, int c) {
+    total = total_;
+    C = c > 0 ? c : max(1, (total_ + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x));
+    chunk = blockIdx.x;
+    in_chunk = 0;
+  }
+  __device__ __forceinline__ int tile() const { return chunk * C + in_chunk; }
+  __device__ __forceinline__ bool valid() const { return chunk * C + in_chunk < total; }
+  __device__ __forceinline__ void next() {
+    if (++in_chunk == C || chunk * C + in_chunk >= total) {
+      in_chunk = 0;
+      chunk += gridDim.x;
+    }
+  }
+};
+
+__device__ __forceinline__ TileDesc load_desc(const Params &p, const TileSeq &s) {
+  if (!s.valid()) return TileDesc{0, 0, -1, -1};
+  const int4 v = __ldg(reinterpret_cast<const int4 *>(p.tdesc) + s.tile());
+  return TileDesc{v.x, v.y, v.z, v.w};
 }
 
 // ---------------------------------------------------------------------------

@@ -22,12 +22,6 @@
 
 namespace nsa {
 
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Pipeline depths per (d, B_K), bounded by 227 KB of shared memory: Q stages,
 // K/V stages and output staging slots per softmax warpgroup (one 64-column block
 // of 128 rows each; two let a warpgroup fill one while the TMA store of the other
@@ -66,32 +60,6 @@ struct FwdSmem {
 // warps 0-3 Q producers, warp 4 MMA, warp 5 TMEM owner, warp 6 K/V producer,
 // warps 8-11 / 12-15 two softmax WGs
 constexpr int kFwdThreads = 512;
-
-// The tiles of one CTA: chunks of `C` consecutive tiles, chunk c going to CTA
-// c % gridDim.x.  C = 0 means one contiguous range per CTA.
-struct TileSeq {
-  int total, C, chunk, in_chunk;
-  __device__ __forceinline__ void init(int total_, int c) {
-    total = total_;
-    C = c > 0 ? c : max(1, (total_ + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x));
-    chunk = blockIdx.x;
-    in_chunk = 0;
-  }
-  __device__ __forceinline__ int tile() const { return chunk * C + in_chunk; }
-  __device__ __forceinline__ bool valid() const { return chunk * C + in_chunk < total; }
-  __device__ __forceinline__ void next() {
-    if (++in_chunk == C || chunk * C + in_chunk >= total) {
-      in_chunk = 0;
-      chunk += gridDim.x;
-    }
-  }
-};
-
-__device__ __forceinline__ TileDesc load_desc(const Params &p, const TileSeq &s) {
-  if (!s.valid()) return TileDesc{0, 0, -1, -1};
-  const int4 v = __ldg(reinterpret_cast<const int4 *>(p.tdesc) + s.tile());
-  return TileDesc{v.x, v.y, v.z, v.w};
-}
 
 // Persistent, warp-specialised forward main kernel (one CTA per SM).
 //   warps 0-3: producers (as many as Q stages, at most 4) -- warp w gathers the
@@ -635,14 +603,27 @@ bool make_qkv_maps(const Params &p, const void *q, CUtensorMap *mq, CUtensorMap 
          encode_map(mv, f16, 3, p.v, kdims, kstr, kbox);
 }
 
-// Tensor map of the compact partial buffer: [max_tiles * 128 rows, d], box =
-// 32 rows x 64 columns (one warp's rows), 128-byte swizzle (the staging layout).
-static bool make_obuf_map(const Params &p, int64_t max_tiles, CUtensorMap *mo) {
+// Tensor map of a tile-padded compact buffer (forward partial O, backward partial
+// dQ): [max_tiles * 128 rows, d], box = 32 rows x 64 columns (one warp's rows),
+// 128-byte swizzle (the staging layout).
+bool make_rows_map(const Params &p, void *base, int64_t max_tiles, CUtensorMap *m) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.d),
                               static_cast<cuuint64_t>(max_tiles) * kTileRows};
   const cuuint64_t str[1] = {static_cast<cuuint64_t>(p.d) * 2};
   const cuuint32_t box[2] = {64, 32};
-  return encode_map(mo, p.dtype == NSA_FP16, 2, p.obuf, dims, str, box);
+  return encode_map(m, p.dtype == NSA_FP16, 2, base, dims, str, box);
+}
+
+// Tensor maps of k and v alone (the backward gathers q and dO with cp.async).
+bool make_kv_maps(const Params &p, CUtensorMap *mk, CUtensorMap *mv) {
+  const bool f16 = p.dtype == NSA_FP16;
+  const cuuint64_t kdims[3] = {static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(p.h_k),
+                               static_cast<cuuint64_t>(p.n)};
+  const cuuint64_t kstr[2] = {static_cast<cuuint64_t>(p.d) * 2,
+                              static_cast<cuuint64_t>(p.h_k) * p.d * 2};
+  const cuuint32_t kbox[3] = {64, 1, static_cast<cuuint32_t>(p.block)};
+  return encode_map(mk, f16, 3, p.k, kdims, kstr, kbox) &&
+         encode_map(mv, f16, 3, p.v, kdims, kstr, kbox);
 }
 
 template <int D, int BK, bool kFp16>
@@ -650,7 +631,7 @@ static cudaError_t run_fwd(const Params &p, int num_sms, int64_t max_tiles, cuda
                            void (*mark)(int, cudaStream_t, bool)) {
   using L = FwdSmem<D, BK>;
   CUtensorMap mq, mk, mv, mo;
-  if (!make_qkv_maps(p, p.q, &mq, &mk, &mv) || !make_obuf_map(p, max_tiles, &mo))
+  if (!make_qkv_maps(p, p.q, &mq, &mk, &mv) || !make_rows_map(p, p.obuf, max_tiles, &mo))
     return cudaErrorInvalidValue;
   // One CTA per SM: it owns all 512 TMEM columns.
   const uint32_t smem = L::kBytes > 120u * 1024u ? L::kBytes : 120u * 1024u;

@@ -360,6 +360,7 @@ __global__ void __launch_bounds__(256) tile_desc_kernel(Params p) {
     const int64_t left = rows - (int64_t)j * kTileRows;
     const int32_t nr = static_cast<int32_t>(left < kTileRows ? left : kTileRows);
     p.tdesc[t0 + j] = TileDesc{q_off, j * kTileRows, key0, h | (nr << 16)};
+    p.tseg[t0 + j] = h * nb + gb;
   }
 }
 

@@ -85,12 +85,16 @@ def test_validation_returns_before_launch(lib):
     st = lib.nsa_sel_attn_fwd(ctypes.byref(d), fake, fake, fake, fake, fake, float("nan"), fake,
                               fake, fake, 1 << 40, None)
     assert st == 1                       # non-finite scale
-    d256 = _dims(head_dim=256)
+    d256 = _dims(head_dim=256, block_size=128)
     st = lib.nsa_sel_attn_bwd(ctypes.byref(d256), fake, fake, fake, fake, fake, 0.1, fake, fake,
                               fake, fake, fake, fake, fake, 1 << 40, 0, None)
-    assert st == 2                       # backward envelope is d <= 128
+    assert st == 2                       # backward with d = 256 needs B_K <= 64
     st = lib.nsa_sel_attn_index(None, fake, fake, fake, 1 << 40, None)
     assert st == 1
+    d128 = _dims(head_dim=128, block_size=128)   # attention kernels not offered for this pair
+    st = lib.nsa_sel_attn_fwd(ctypes.byref(d128), fake, fake, fake, fake, fake, 0.1, fake, fake,
+                              fake, 1 << 40, None)
+    assert st == 2
 
 
 def test_status_strings_and_kernel_names(lib):

@@ -37,11 +37,56 @@ def _check(cfg, inp, grads):
         assert err <= GRAD_REL_L2, f"{cfg.name} {name}: rel-L2 {err:.3e}"
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("block", [32, 64, 128])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-def test_backward_small_ragged(block, dtype):
-    cfg = WorkloadConfig("bwd_small", (300, 1, 517, 64, 250), 2, 3, 128, block, 5, dtype,
+def test_backward_small_ragged(d, block, dtype):
+    # several sequences with ragged tails, g = 3 (tiles split tokens' heads), T = 5
+    if (d == 256 and block == 128) or (d == 128 and block == 128):
+        pytest.skip("outside the supported envelope (rejected, see the rejection tests)")
+    cfg = WorkloadConfig("bwd_small", (300, 1, 517, 64, 250), 2, 3, d, block, 5, dtype,
                          "uniform", 1.0, 5, with_dout=True)
+    inp = make_inputs(cfg)
+    _check(cfg, inp, _run(cfg, inp))
+
+
+def test_d128_b128_is_rejected():
+    import block_sparse_attention_nsa_gb300 as nsa
+    cfg = WorkloadConfig("rej128", (200,), 1, 2, 128, 128, 4, "bf16", "uniform", 1.0, 3,
+                         with_dout=True)
+    inp = make_inputs(cfg)
+    d = to_device(inp)
+    with pytest.raises(nsa.NsaError) as e:
+        nsa.fwd(d["q"], d["k"], d["v"], d["sel_idx"], d["cu_seqlens"], cfg.block, cfg.scale)
+    assert e.value.code == 2
+
+
+def test_backward_d256_b128_is_rejected():
+    import block_sparse_attention_nsa_gb300 as nsa
+    cfg = WorkloadConfig("bwd_rej", (200,), 1, 2, 256, 128, 4, "fp16", "uniform", 1.0, 3,
+                         with_dout=True)
+    inp = make_inputs(cfg)
+    d = to_device(inp)
+    out = torch.zeros_like(d["q"])
+    lse = torch.zeros((cfg.h_q, cfg.n), dtype=torch.float32, device="cuda")
+    with pytest.raises(nsa.NsaError) as e:
+        nsa.bwd(d["q"], d["k"], d["v"], d["sel_idx"], d["cu_seqlens"], cfg.block, cfg.scale, out,
+                lse, d["dout"])
+    assert e.value.code == 2
+
+
+def test_backward_tiny_config():
+    # the tiny workload (d = 64, B_K = 32, T = 4, g = 2) with dO ~ N(0, 1)
+    cfg = CONFIGS["tiny"]
+    inp = make_inputs(cfg, with_dout=True)
+    _check(cfg, inp, _run(cfg, inp))
+
+
+def test_backward_varlen_shaped_d256_fp16():
+    # the varlen workload's shape (4 packed sequences, h_k = 2, g = 4, d = 256, fp16,
+    # N(0, 0.5), uniform selection) with every length divided by 8
+    cfg = WorkloadConfig("bwd_varlen8", (2048, 4096, 1024, 1024), 2, 4, 256, 64, 16, "fp16",
+                         "uniform", CONFIGS["varlen"].std, 1013, with_dout=True)
     inp = make_inputs(cfg)
     _check(cfg, inp, _run(cfg, inp))
 

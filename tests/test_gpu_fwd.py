@@ -65,6 +65,12 @@ def test_forward_shapes_ragged(d, block, dtype):
     cfg = WorkloadConfig("ragged", (300, 1, 517, 64, 0, 250), 2, 3, d, block, 5, dtype,
                          "uniform", 1.0, 77)
     inp = make_inputs(cfg)
+    if d == 128 and block == 128:
+        import block_sparse_attention_nsa_gb300 as nsa
+        with pytest.raises(nsa.NsaError) as e:      # outside the supported envelope
+            _run(cfg, inp)
+        assert e.value.code == 2
+        return
     out, lse = _run(cfg, inp)
     ref_out, ref_lse = oracle.fwd(inp["cu_seqlens"], cfg.block, inp["sel_idx"], inp["q"],
                                   inp["k"], inp["v"], cfg.scale)
