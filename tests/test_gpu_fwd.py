@@ -1,8 +1,8 @@
 """GPU forward vs the fp64 oracle on the same seeded inputs (through the C ABI).
 
-Small workloads are compared element by element; the 64K and varlen workloads
-at full size, in the launch configuration the benchmark times, on sampled
-(token, query head) rows that the oracle computes one by one."""
+Every workload, the 64K one at g = 1, 2, 4, 8 and the varlen one included, is
+compared element by element over the whole output and lse, in the launch
+configuration the benchmark times."""
 import numpy as np
 import pytest
 import torch
@@ -34,27 +34,36 @@ def test_forward_full_compare(name):
 
 
 @pytest.mark.parametrize("g", [1, 2, 4, 8])
-def test_forward_64k_sampled(g):
+def test_forward_64k_full(g):
+    # the 64K workload at every group size, in the benchmark's launch configuration,
+    # compared element by element over the whole output and lse
     cfg = CONFIGS["fwd64k"].with_g(g)
     inp = make_inputs(cfg)
     out, lse = _run(cfg, inp)
-    rows = sample_rows(cfg.n, cfg.h_q, 3000, seed=g, block=cfg.block)
-    ref_o, ref_l = oracle.fwd_rows(inp["cu_seqlens"], cfg.block, inp["sel_idx"], inp["q"],
-                                   inp["k"], inp["v"], cfg.scale, rows)
-    o = out[rows[:, 0], rows[:, 1]]
-    l = lse[rows[:, 1], rows[:, 0]]
-    check_forward(o, l, ref_o, ref_l, cfg.name)
+    ref_out, ref_lse = oracle.fwd(inp["cu_seqlens"], cfg.block, inp["sel_idx"], inp["q"],
+                                  inp["k"], inp["v"], cfg.scale)
+    check_forward(out, lse, ref_out, ref_lse, cfg.name)
 
 
-def test_forward_varlen_sampled():
+def test_forward_varlen_full():
     cfg = CONFIGS["varlen"]
     inp = make_inputs(cfg)
     out, lse = _run(cfg, inp)
-    rows = sample_rows(cfg.n, cfg.h_q, 3000, seed=7, seqlens=list(cfg.seqlens), block=cfg.block)
+    ref_out, ref_lse = oracle.fwd(inp["cu_seqlens"], cfg.block, inp["sel_idx"], inp["q"],
+                                  inp["k"], inp["v"], cfg.scale)
+    check_forward(out, lse, ref_out, ref_lse, "varlen")
+
+
+def test_forward_64k_sampled_boundaries():
+    # quick tier: sequence edges and block boundaries of the 64K workload at g = 4
+    cfg = CONFIGS["fwd64k"].with_g(4)
+    inp = make_inputs(cfg)
+    out, lse = _run(cfg, inp)
+    rows = sample_rows(cfg.n, cfg.h_q, 500, seed=4, block=cfg.block)
     ref_o, ref_l = oracle.fwd_rows(inp["cu_seqlens"], cfg.block, inp["sel_idx"], inp["q"],
                                    inp["k"], inp["v"], cfg.scale, rows)
     check_forward(out[rows[:, 0], rows[:, 1]], lse[rows[:, 1], rows[:, 0]], ref_o, ref_l,
-                  "varlen")
+                  cfg.name)
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])

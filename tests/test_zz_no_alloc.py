@@ -94,3 +94,39 @@ def test_noalloc_rejects_problems_above_the_limit():
     assert st == 3                       # NSA_ERR_WORKSPACE, nothing launched
     torch.cuda.synchronize()
     assert torch.isnan(out).all()
+
+
+def _status():
+    import block_sparse_attention_nsa_gb300 as nsa
+    lib = nsa.load()
+    fn = lib.nsa_sel_attn_fwd_noalloc_status
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.POINTER(nsa.Dims), ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
+    return fn
+
+
+def test_noalloc_status_reports_a_bad_selection_and_clears():
+    status = _status()
+    cfg = CONFIGS["tiny"]
+    d, dims = _case(cfg)
+    stream = torch.cuda.current_stream().cuda_stream
+    bits = ctypes.c_int32(-1)
+    # a clean call first: the word reads 0
+    st, _, _ = _noalloc(d, dims, cfg)
+    assert st == 0
+    assert status(ctypes.byref(dims), stream, ctypes.byref(bits)) == 0 and bits.value == 0
+    # one slot past the sequence's last block: skipped by the kernels, flagged in the word
+    nb = (cfg.n + cfg.block - 1) // cfg.block
+    bad = d["sel_idx"].clone()
+    bad[0, cfg.n - 1, cfg.topk - 1] = nb
+    d_bad = dict(d, sel_idx=bad)
+    st, out, lse = _noalloc(d_bad, dims, cfg)
+    assert st == 0
+    assert status(ctypes.byref(dims), stream, ctypes.byref(bits)) == 5   # NSA_ERR_BAD_INDEX
+    assert bits.value & 1                                                # NSA_DEVERR_BAD_INDEX
+    assert torch.isfinite(out).all()
+    # read and cleared: the next read is clean, and so is the next good call
+    assert status(ctypes.byref(dims), stream, ctypes.byref(bits)) == 0 and bits.value == 0
+    st, _, _ = _noalloc(d, dims, cfg)
+    assert st == 0
+    assert status(ctypes.byref(dims), stream, ctypes.byref(bits)) == 0 and bits.value == 0
