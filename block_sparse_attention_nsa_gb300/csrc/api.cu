@@ -100,6 +100,12 @@ nsa_status check_dims(const nsa_sel_attn_dims *d, bool bwd) {
 #define NSA_FWD_CHUNK 8
 #endif
 constexpr int kFwdChunk = NSA_FWD_CHUNK;
+// Backward schedule: the same dealing; the backward also writes one dK/dV partial per
+// (segment, chunk) pair, so longer chunks mean fewer partials.
+#ifndef NSA_BWD_CHUNK
+#define NSA_BWD_CHUNK 16
+#endif
+constexpr int kBwdChunk = NSA_BWD_CHUNK;
 
 // Shared memory the index builder may use per CTA (count: one int per block;
 // scatter: one bit per (token, block) of the CTA's token tile).
@@ -174,9 +180,9 @@ nsa_status make_layout(const nsa_sel_attn_dims *d, Layout *L) {
   L->mlbuf = take(static_cast<size_t>(L->max_wtiles) * kTileRows * 8);
   L->fwd_end = o;
   o = scratch;
-  // backward: one dK/dV partial per (segment, CTA) pair a segment's tiles span;
-  // the CTAs take contiguous tile ranges, so that is at most segments + CTAs
-  L->max_parts = h_k * L->nb_max + kMaxBwdCtas;
+  // backward: one dK/dV partial per (segment, chunk) pair a segment's tiles meet, at
+  // most segments + chunk boundaries
+  L->max_parts = h_k * L->nb_max + L->max_wtiles / kBwdChunk + 1;
   L->dstat = take(4 * static_cast<size_t>(N) * d->h_q);
   L->part_off = take(4 * nseg1);
   L->dqbuf = take(static_cast<size_t>(L->max_wtiles) * kTileRows * d->head_dim * 2);
@@ -222,6 +228,7 @@ void fill_params(Params *p, const nsa_sel_attn_dims *d, const Layout &L, void *w
   p->n_w = L.n_w;
   p->wave_tiles = L.wave_tiles;
   p->fwd_chunk = kFwdChunk;
+  p->bwd_chunk = kBwdChunk;
   p->obuf = w + L.obuf;
   p->mlbuf = reinterpret_cast<float2 *>(w + L.mlbuf);
   p->dstat = reinterpret_cast<float *>(w + L.dstat);

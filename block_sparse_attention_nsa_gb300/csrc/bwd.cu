@@ -6,14 +6,15 @@
 //
 //   bwd_pre   : D[hq, t] = sum_d dO * O (fp32); the first dK/dV partial slot of
 //               every (KV head, block) segment.
-//   bwd_main  : persistent and warp-specialised; each CTA takes one contiguous
-//               range of tiles.  Per tile, on tcgen05 with TMEM accumulators:
-//               S = Q K_b^T and dP = dO V_b^T; in registers P = exp2(S*scale*log2e
-//               - lse*log2e) (causal mask) and dS = P (dP - D), written to shared
-//               memory in 16 bits; dV_b^T += dO^T P and dK_b^T += Q^T dS stay in
-//               TMEM over the whole run of tiles of one block; dQ_part = dS K_b
-//               goes to a tile-padded compact buffer.  At the end of a run the
-//               dK_b, dV_b partials are written once (one slot per block and CTA).
+//   bwd_main  : persistent and warp-specialised; tiles are dealt to the CTAs in
+//               chunks of consecutive tiles.  Per tile, on tcgen05 with TMEM
+//               accumulators: S = Q K_b^T and dP = dO V_b^T; in registers P =
+//               exp2(S*scale*log2e - lse*log2e) (causal mask) and dS = P (dP - D),
+//               written to shared memory in 16 bits; dV_b^T += dO^T P and dK_b^T +=
+//               Q^T dS stay in TMEM over a run of tiles of one block inside one
+//               chunk; dQ_part = dS K_b goes to a tile-padded compact buffer.  At the
+//               end of a run the dK_b, dV_b partials are written once (one slot per
+//               block and chunk).
 //   bwd_dq    : per (token, query head), dq = scale * sum of its <= T dQ partials.
 //   bwd_dkv   : per block, dk = scale * sum of its partials of dK, dv = that of dV;
 //               blocks nobody selected get zeros.
@@ -46,14 +47,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(Params p) {
   if (lane == 0) p.dstat[(int64_t)hq * p.n + t] = acc;
 }
 
-// First dK/dV partial slot of every segment.  The main kernel's CTA c takes the
-// tiles [c * per, (c + 1) * per), per = ceil(total / grid); a segment whose tiles
-// run over CTAs c0 .. c1 gets c1 - c0 + 1 slots.  One block of 1024 threads.
-__global__ void __launch_bounds__(1024) bwd_parts_kernel(Params p, int grid) {
+// First dK/dV partial slot of every segment.  The main kernel deals tiles in
+// chunks of C = p.bwd_chunk consecutive tiles and writes one dK/dV partial per
+// (segment, chunk) pair the segment's tiles meet, so a segment with tiles
+// [a, b) gets (b - 1) / C - a / C + 1 slots.  One block of 1024 threads.
+__global__ void __launch_bounds__(1024) bwd_parts_kernel(Params p) {
   __shared__ int32_t sums[32];
   const int nseg = p.h_k * (*p.nb);
-  const int total = p.tile_off[nseg];
-  const int per = total > 0 ? (total + grid - 1) / grid : 1;
+  const int per = p.bwd_chunk;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int each = (nseg + 1023) / 1024;
   const int i0 = min(nseg, tid * each), i1 = min(nseg, i0 + each);
@@ -99,29 +100,35 @@ struct BwdCfg {
   static constexpr int DQC = D < 128 ? D : 128;  // dQ columns per half
   static constexpr int NKV = BK < 64 ? 64 : BK;  // P / dS columns: at least one 128-byte atom
   static constexpr int QS = (D == 256 || (D == 128 && BK == 128)) ? 1 : 2;   // Q/dO stages
-  static constexpr int NPW = QS;                 // producer warps, one per stage
+  // compute warpgroups, each with its own S/dP (TMEM) and P/dS (shared memory)
+  // buffers and taking every NWG-th tile; two where TMEM and shared memory have room
+  static constexpr int NWG = (D <= 128 && BK <= 64) ? 2 : 1;
+  static constexpr int NPW = 4;                  // producer warps
+  static constexpr int WPS = NPW / QS;           // producer warps per Q/dO stage
+  static constexpr int RW = 128 / WPS;           // tile rows gathered per producer warp
+  // warps 0-3 producers, 4 MMA, 5 TMEM, 6 K/V, 8-11 (and 12-15) compute warpgroups
+  static constexpr int kThreads = 256 + 128 * NWG;
   static constexpr uint32_t kQ = 128u * DW * 2u;        // one Q (or dO) tile
   static constexpr uint32_t kK = uint32_t(BK) * D * 2u;  // K or V
   static constexpr uint32_t kP = 128u * NKV * 2u;       // P or dS (also dQ staging)
   static constexpr uint32_t kOffQ = 0;                   // stage s: Q at 2 s kQ, dO at (2 s + 1) kQ
   static constexpr uint32_t kOffK = QS * 2 * kQ;
   static constexpr uint32_t kOffV = kOffK + kK;
-  static constexpr uint32_t kOffP = kOffV + kK;
-  static constexpr uint32_t kOffDS = kOffP + kP;
-  static constexpr uint32_t kBytes = kOffDS + kP + 1024;
+  static constexpr uint32_t kOffP = kOffV + kK;          // warpgroup w: P at 2 w kP, dS after it
+  static constexpr uint32_t kBytes = kOffP + NWG * 2 * kP + 1024;
   static_assert(kBytes <= 227u * 1024u, "shared memory budget");
   static_assert(2 * kP >= 128u * DQC * 2u, "P/dS buffers double as dQ staging");
-  // TMEM: S [0, BK), dP [BK, 2 BK); dQ after them, or over them when short of columns;
-  // dV^T then dK^T (NH lane halves of NKV columns each)
-  static constexpr bool kDqAlias = 2 * BK + DQC + 2 * NH * NKV > 512;
-  static constexpr int kTmDQ = kDqAlias ? 0 : 2 * BK;
-  static constexpr int kTmDV = kDqAlias ? 2 * BK : 2 * BK + DQC;
+  // TMEM: warpgroup w's S at [2 w BK, 2 w BK + BK) and dP at [2 w BK + BK, 2 (w + 1) BK);
+  // dQ after them, or over them when short of columns (one warpgroup only); dV^T then
+  // dK^T (NH lane halves of NKV columns each)
+  static constexpr bool kDqAlias = NWG * 2 * BK + DQC + 2 * NH * NKV > 512;
+  static_assert(!kDqAlias || NWG == 1, "an aliased dQ needs a single warpgroup");
+  static constexpr int kTmDQ = kDqAlias ? 0 : NWG * 2 * BK;
+  static constexpr int kTmDV = kDqAlias ? 2 * BK : NWG * 2 * BK + DQC;
   static constexpr int kTmDK = kTmDV + NH * NKV;
   static_assert(kTmDK + NH * NKV <= 512, "TMEM budget");
   static_assert(!kDqAlias || DQC <= 2 * BK, "aliased dQ fits the S/dP columns");
 };
-
-constexpr int kBwdThreads = 384;   // warps 0-1 producers, 4 MMA, 5 TMEM, 6 K/V, 8-11 compute
 
 template <bool kFp16>
 __device__ __forceinline__ void st_row_chunks(uint32_t tile, int row, int chunk0, const float *v32) {
@@ -137,39 +144,45 @@ __device__ __forceinline__ void st_row_chunks(uint32_t tile, int row, int chunk0
   }
 }
 
-// Persistent, warp-specialised backward main kernel (one CTA per SM).
-//   warps 0..NPW-1: producers -- warp w gathers the Q and dO rows of tiles w,
-//     w + NPW, ... by cp.async into the 128-byte-swizzled operand layout and
-//     arrives when its own copies have landed;
-//   warp 6 (one thread): K_b and V_b by TMA, once per run of tiles of a block;
-//   warp 4 (one thread): tcgen05 MMAs, per tile S, dP; then dV^T, dK^T, dQ;
-//   warps 8-11: P and dS, the dQ epilogue (through the P/dS buffers, which are
-//     free once the dQ MMA has read them) and, at the end of a run, dK/dV out.
+// Persistent, warp-specialised backward main kernel (one CTA per SM).  Tiles are
+// dealt to the CTAs in chunks of p.bwd_chunk consecutive tiles, round-robin, so all
+// CTAs work on neighbouring blocks at any time and the Q/dO rows they gather stay
+// L2-resident.  A run is a CTA's consecutive tiles of one (KV head, block) inside one
+// chunk: K/V is loaded, and dK/dV accumulated in TMEM, once per run.
+//   warps 0-3: producers -- the WPS warps of a Q/dO stage gather RW rows each of
+//     that stage's tiles by cp.async into the 128-byte-swizzled operand layout and
+//     arrive when their own copies have landed;
+//   warp 6 (one thread): K_b and V_b by TMA, once per run;
+//   warp 4 (one thread): tcgen05 MMAs, per tile S and dP (interleaved: two
+//     independent accumulators), then dV^T, dK^T and dQ.  S/dP of later tiles are
+//     issued as soon as their Q/dO rows have landed, while it waits for P/dS;
+//   warps 8-11 (and 12-15): compute warpgroup w takes tiles w, w + NWG, ...: P and
+//     dS of its tile, the dQ epilogue (through its P/dS buffers, free once the dQ
+//     MMA has read them) and, at the end of a run, dK/dV out.
 // mbarriers hand each buffer between roles; every wait is bounded.
 template <int D, int BK, bool kFp16>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(BwdCfg<D, BK>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_dq, Params p) {
   using L = BwdCfg<D, BK>;
-  constexpr int QS = L::QS, NPW = L::NPW, NH = L::NH, DQC = L::DQC, NKV = L::NKV;
+  constexpr int QS = L::QS, NWG = L::NWG, NH = L::NH, DQC = L::DQC, NKV = L::NKV;
   constexpr int kCB = D / 64;
   constexpr uint32_t kIdescS = idesc_f16(128, BK, false, false, kFp16);     // S, dP
   constexpr uint32_t kIdescKV = idesc_f16(128, NKV, true, true, kFp16);     // dV^T, dK^T
   constexpr uint32_t kIdescQ = idesc_f16(128, DQC, false, true, kFp16);     // dQ
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t qd_full[QS], qd_empty[QS], kv_full, kv_empty, sdp_full, sdp_free,
-      pds_full, dq_full, dq_free, dkv_free;
-  // K/V flags of the tile in each stage: bit 8 first tile of its block's run, bit 9 last
+  __shared__ uint64_t qd_full[QS], qd_empty[QS], kv_full, kv_empty, sdp_full[NWG],
+      sdp_free[NWG], pds_full[NWG], dq_full[NWG], dq_free, dkv_free;
+  // K/V flags of the tile in each stage: bit 8 first tile of its run, bit 9 last
   __shared__ uint32_t qd_flags[QS];
   __shared__ uint32_t tmem_base;
   __shared__ int fail;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   const uint32_t sQ0 = smem_u32(smem + L::kOffQ), sK = smem_u32(smem + L::kOffK),
-                 sV = smem_u32(smem + L::kOffV), sP = smem_u32(smem + L::kOffP),
-                 sDS = smem_u32(smem + L::kOffDS);
+                 sV = smem_u32(smem + L::kOffV), sP0 = smem_u32(smem + L::kOffP);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // zero the Q/dO stages once: with d = 64 their upper 64 columns stay zero
@@ -180,13 +193,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   if (warp == 5) tmem_alloc(&tmem_base, 512);
   if (tid == 0) {
-    for (int i = 0; i < QS; ++i) { mbar_init(&qd_full[i], 32); mbar_init(&qd_empty[i], 1); }
+    for (int i = 0; i < QS; ++i) {
+      mbar_init(&qd_full[i], 32 * L::WPS);
+      mbar_init(&qd_empty[i], 1);
+    }
     mbar_init(&kv_full, 1);
     mbar_init(&kv_empty, 1);
-    mbar_init(&sdp_full, 1);
-    mbar_init(&sdp_free, 128);
-    mbar_init(&pds_full, 128);
-    mbar_init(&dq_full, 1);
+    for (int w = 0; w < NWG; ++w) {
+      mbar_init(&sdp_full[w], 1);
+      mbar_init(&sdp_free[w], 128);
+      mbar_init(&pds_full[w], 128);
+      mbar_init(&dq_full[w], 1);
+    }
     mbar_init(&dq_free, 128);
     mbar_init(&dkv_free, 128);
     fail = 0;
@@ -195,29 +213,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tS = tmem_base, tDP = tmem_base + BK, tDQ = tmem_base + L::kTmDQ,
-                 tDV = tmem_base + L::kTmDV, tDK = tmem_base + L::kTmDK;
+  const uint32_t tDQ = tmem_base + L::kTmDQ, tDV = tmem_base + L::kTmDV,
+                 tDK = tmem_base + L::kTmDK;
   const int total = p.tile_off[p.h_k * (*p.nb)];
-  auto same_kv = [](const TileDesc &a, const TileDesc &b) {
-    return (a.hn & 0xffff) == (b.hn & 0xffff) && a.key0 == b.key0;
+  const int C = p.bwd_chunk;
+  auto same_run = [C](int ta, const TileDesc &a, int tb, const TileDesc &b) {
+    return (a.hn & 0xffff) == (b.hn & 0xffff) && a.key0 == b.key0 && ta / C == tb / C;
   };
 
-  if (warp < NPW) {
+  if (warp < L::NPW) {
     // ------------------------------ producers ------------------------------
+    constexpr int WPS = L::WPS, RW = L::RW, NJ = RW / 32;
     constexpr int kCPR = D / 8;           // 16-byte chunks per row
     constexpr int kRPI = 32 / kCPR;       // rows per warp instruction
-    constexpr int kIns = 128 / kRPI;      // warp instructions per tile and tensor
+    constexpr int kIJ = 32 / kRPI;        // warp instructions per 32 rows and tensor
+    const int qs = warp / WPS, part = warp % WPS;   // stage, and rows [part RW, part RW + RW)
     TileSeq seq;
-    seq.init(total, 0);
-    for (int k = 0; k < warp; ++k) seq.next();
+    seq.init(total, C);
+    for (int k = 0; k < qs; ++k) seq.next();
     TileSeq prv;
-    prv.init(total, 0);
-    for (int k = 0; k + 1 < warp; ++k) prv.next();
+    prv.init(total, C);
+    for (int k = 0; k + 1 < qs; ++k) prv.next();
     const int oob_row = p.n * p.h_q;
     const uint16_t *gq = static_cast<const uint16_t *>(p.q);
     const uint16_t *gdo = static_cast<const uint16_t *>(p.dout);
     const uint64_t keep = l2_evict_last();
-    int li = warp;
+    const uint32_t stq = sQ0 + 2 * qs * L::kQ, stdo = stq + L::kQ;
+    int li = qs;
     while (seq.valid()) {
       const TileDesc dc = load_desc(p, seq);
       TileSeq sn = seq;
@@ -225,10 +247,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const TileDesc dn = load_desc(p, sn);
       const TileDesc dp = li > 0 ? load_desc(p, prv) : TileDesc{0, 0, -1, -1};
       const int h = dc.hn & 0xffff, nrows = dc.hn >> 16;
-      int rid[4];
+      int rid[NJ];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int r = j * 32 + lane;
+      for (int j = 0; j < NJ; ++j) {
+        const int r = part * RW + j * 32 + lane;
         rid[j] = oob_row;
         if (r < nrows) {
           const int rr = dc.row0 + r;
@@ -236,17 +258,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           rid[j] = t * p.h_q + h * p.g + rr % p.g;
         }
       }
-      const bool first = li == 0 || !same_kv(dp, dc);
-      const bool last = !sn.valid() || !same_kv(dn, dc);
-      const int qs = li % QS;
+      const bool first = li == 0 || !same_run(prv.tile(), dp, seq.tile(), dc);
+      const bool last = !sn.valid() || !same_run(seq.tile(), dc, sn.tile(), dn);
       if (li >= QS) mbar_wait_sticky(&qd_empty[qs], ((li / QS) - 1) & 1, p.status, &fail);
-      const uint32_t stq = sQ0 + 2 * qs * L::kQ, stdo = stq + L::kQ;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < NJ; ++j) {
 #pragma unroll 4
-        for (int k = 0; k < kIns / 4; ++k) {
-          const int r = (j * (kIns / 4) + k) * kRPI + lane / kCPR;
-          const int id = __shfl_sync(0xffffffffu, rid[j], r & 31);
+        for (int k = 0; k < kIJ; ++k) {
+          const int r32 = k * kRPI + lane / kCPR;          // row within this 32-row group
+          const int id = __shfl_sync(0xffffffffu, rid[j], r32);
+          const int r = part * RW + j * 32 + r32;          // tile row
           const int chunk = lane % kCPR;
           const bool in = id < oob_row;
           const int64_t off = in ? (int64_t)id * D + chunk * 8 : 0;
@@ -256,28 +277,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       cp_async_commit();
-      if (lane == 0) qd_flags[qs] = (first ? 0x100u : 0u) | (last ? 0x200u : 0u);
+      if (lane == 0 && part == 0) qd_flags[qs] = (first ? 0x100u : 0u) | (last ? 0x200u : 0u);
       cp_async_wait_all();
       fence_proxy_async_smem();
       mbar_arrive(&qd_full[qs]);
+      // this stage's next tile is li + QS; its predecessor is li + QS - 1
       prv = seq;
 #pragma unroll
-      for (int k = 0; k + 1 < NPW; ++k) prv.next();
+      for (int k = 0; k + 1 < QS; ++k) prv.next();
       seq = prv;
       seq.next();
-      li += NPW;
+      li += QS;
     }
   } else if (warp == 6) {
     // ------------------------------ K/V producer ------------------------------
     if (lane == 0) {
       const uint64_t keep = l2_evict_last();
       TileSeq seq;
-      seq.init(total, 0);
-      int kv_n = 0, prev_h = -1, prev_key0 = -1;
+      seq.init(total, C);
+      int kv_n = 0, tprev = -1;
+      TileDesc dprev{0, 0, -1, -1};
       while (seq.valid()) {
         const TileDesc dc = load_desc(p, seq);
-        const int h = dc.hn & 0xffff;
-        if (h != prev_h || dc.key0 != prev_key0) {
+        const int t = seq.tile(), h = dc.hn & 0xffff;
+        if (tprev < 0 || !same_run(tprev, dprev, t, dc)) {
           if (kv_n >= 1) mbar_wait_sticky(&kv_empty, (kv_n - 1) & 1, p.status, &fail);
           mbar_arrive_expect_tx(&kv_full, 2u * L::kK);
 #pragma unroll
@@ -286,9 +309,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_load_3d_hint(sV + cb * BK * 128, &tm_v, cb * 64, h, dc.key0, &kv_full, keep);
           }
           ++kv_n;
-          prev_h = h;
-          prev_key0 = dc.key0;
         }
+        tprev = t;
+        dprev = dc;
         seq.next();
       }
     }
@@ -296,37 +319,79 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
       TileSeq seq;
-      seq.init(total, 0);
+      seq.init(total, C);
       int n = 0;
       for (TileSeq c = seq; c.valid(); c.next()) ++n;
-      uint32_t flags[2] = {0u, 0u};
-      int s_kv = 0, runs = 0, dq_n = 0;
-      auto issue_sdp = [&](int i) {
-        const int qs = i % QS;
-        mbar_wait_sticky(&qd_full[qs], (i / QS) & 1, p.status, &fail);
-        const uint32_t f = qd_flags[qs];
-        flags[i & 1] = f;
-        if (f & 0x100u) {
-          mbar_wait_sticky(&kv_full, s_kv & 1, p.status, &fail);
-          ++s_kv;
-        }
-        if (i > 0) mbar_wait_sticky(&sdp_free, (i - 1) & 1, p.status, &fail);
-        tc_fence_after();
-        const uint32_t stq = sQ0 + 2 * qs * L::kQ, stdo = stq + L::kQ;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_f16(tS, desc_kmajor(stq, 128, kk), desc_kmajor(sK, BK, kk), kIdescS, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_f16(tDP, desc_kmajor(stdo, 128, kk), desc_kmajor(sV, BK, kk), kIdescS, kk > 0);
-        mma_commit(&sdp_full);
+      // K/V flags of the tiles in flight (tiles i .. i + NWG), kept in registers by
+      // tile index mod 4
+      uint32_t fl0 = 0u, fl1 = 0u, fl2 = 0u, fl3 = 0u;
+      auto fl_get = [&](int j) -> uint32_t {
+        const int s = j & 3;
+        return s == 0 ? fl0 : (s == 1 ? fl1 : (s == 2 ? fl2 : fl3));
       };
-      if (n > 0) issue_sdp(0);
+      auto fl_set = [&](int j, uint32_t f) {
+        const int s = j & 3;
+        if (s == 0) fl0 = f;
+        else if (s == 1) fl1 = f;
+        else if (s == 2) fl2 = f;
+        else fl3 = f;
+      };
+      int s_kv = 0, runs = 0, dq_n = 0;
+      int s_next = 0;    // next tile whose S/dP is to be issued
+      int i_done = -1;   // last tile whose dV/dK/dQ MMAs (and K/V release) are issued
+      // Issues S/dP of tiles s_next .. i_done + NWG.  Tile i_done + 1 is needed next,
+      // so it is waited for; later tiles only if their Q/dO rows are in already.  A
+      // tile that starts a new run waits until every earlier tile is issued, since
+      // the K/V stage is released by the last tile of the previous run.
+      auto try_issue = [&]() {
+        while (s_next < n && s_next <= i_done + NWG) {
+          const int j = s_next, qs = j % QS, w = j % NWG;
+          const bool must = j == i_done + 1;
+          if (must) mbar_wait_sticky(&qd_full[qs], (j / QS) & 1, p.status, &fail);
+          else if (!mbar_test_wait(smem_u32(&qd_full[qs]), (j / QS) & 1)) break;
+          const uint32_t f = qd_flags[qs];
+          if ((f & 0x100u) && !must) break;
+          fl_set(j, f);
+          if (f & 0x100u) {
+            mbar_wait_sticky(&kv_full, s_kv & 1, p.status, &fail);
+            ++s_kv;
+          }
+          if (j >= NWG) mbar_wait_sticky(&sdp_free[w], ((j / NWG) - 1) & 1, p.status, &fail);
+          // an aliased dQ occupies the S/dP columns until the epilogue has read it
+          if (L::kDqAlias && dq_n > 0)
+            mbar_wait_sticky(&dq_free, (dq_n - 1) & 1, p.status, &fail);
+          tc_fence_after();
+          const uint32_t stq = sQ0 + 2 * qs * L::kQ, stdo = stq + L::kQ;
+          const uint32_t tSw = tmem_base + w * 2 * BK, tDPw = tSw + BK;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            mma_f16(tSw, desc_kmajor(stq, 128, kk), desc_kmajor(sK, BK, kk), kIdescS, kk > 0);
+            mma_f16(tDPw, desc_kmajor(stdo, 128, kk), desc_kmajor(sV, BK, kk), kIdescS, kk > 0);
+          }
+          mma_commit(&sdp_full[w]);
+          ++s_next;
+        }
+      };
+      try_issue();
       for (int i = 0; i < n; ++i) {
-        const uint32_t f = flags[i & 1];
-        const int qs = i % QS;
+        const int qs = i % QS, w = i % NWG;
         const uint32_t stq = sQ0 + 2 * qs * L::kQ, stdo = stq + L::kQ;
-        mbar_wait_sticky(&pds_full, i & 1, p.status, &fail);
+        const uint32_t sPw = sP0 + w * 2 * L::kP, sDSw = sPw + L::kP;
+        // wait for P/dS(i), issuing S/dP of later tiles as their rows land
+        {
+          const uint32_t a = smem_u32(&pds_full[w]), par = (i / NWG) & 1;
+          if (!mbar_test_wait(a, par)) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!fail && !mbar_test_wait(a, par)) {
+              try_issue();
+              if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                fail = 1;
+                set_status(p.status, NSA_DEVERR_TIMEOUT);
+              }
+            }
+          }
+        }
+        const uint32_t f = fl_get(i);
         const bool first = (f & 0x100u) != 0;
         if (first) {
           if (runs > 0) mbar_wait_sticky(&dkv_free, (runs - 1) & 1, p.status, &fail);
@@ -340,9 +405,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
             mma_f16(tDV + hh * NKV, desc_mnmajor(stdo + hh * 2 * 128 * 128, 128, ks),
-                    desc_mnmajor(sP, 128, ks), kIdescKV, acc);
+                    desc_mnmajor(sPw, 128, ks), kIdescKV, acc);
             mma_f16(tDK + hh * NKV, desc_mnmajor(stq + hh * 2 * 128 * 128, 128, ks),
-                    desc_mnmajor(sDS, 128, ks), kIdescKV, acc);
+                    desc_mnmajor(sDSw, 128, ks), kIdescKV, acc);
           }
         }
         mma_commit(&qd_empty[qs]);
@@ -353,28 +418,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks)
-            mma_f16(tDQ, desc_kmajor(sDS, 128, ks),
+            mma_f16(tDQ, desc_kmajor(sDSw, 128, ks),
                     desc_mnmajor(sK + hh * 2 * BK * 128, BK, ks), kIdescQ, ks > 0);
-          mma_commit(&dq_full);
+          mma_commit(&dq_full[w]);
           ++dq_n;
         }
         if (f & 0x200u) mma_commit(&kv_empty);
-        if (i + 1 < n) {
-          // an aliased dQ occupies the S/dP columns until the epilogue has read it
-          if (L::kDqAlias) mbar_wait_sticky(&dq_free, (dq_n - 1) & 1, p.status, &fail);
-          issue_sdp(i + 1);
-        }
+        i_done = i;
+        try_issue();
       }
     }
-  } else if (warp >= 8) {
-    // ----------------------------- compute warpgroup -----------------------------
-    const int row = tid - 256;                              // tile row = TMEM lane
+  } else if (warp >= 8 && ((warp - 8) >> 2) < NWG) {
+    // ----------------------------- compute warpgroups -----------------------------
+    const int wg = (warp - 8) >> 2;
+    const int row = (tid - 256) & 127;                      // tile row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem_base + wg * 2 * BK, tDP = tS + BK;
+    const uint32_t sP = sP0 + wg * 2 * L::kP, sDS = sP + L::kP;
     const uint64_t stream = l2_evict_first();
     const float kLog2e = 1.4426950408889634f;
     TileSeq seq;
-    seq.init(total, 0);
-    const int per = seq.C;                                  // tiles per CTA (contiguous)
+    seq.init(total, C);
+    if (wg == 1) seq.next();
     auto row_meta = [&](const TileDesc &d, int &lim, float &lse2, float &dval) {
       const int nrows = d.hn >> 16, h = d.hn & 0xffff;
       lim = -1;
@@ -393,13 +458,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int lim = -1;
     float lse2 = 0.f, dval = 0.f;
     if (seq.valid()) row_meta(dsc, lim, lse2, dval);
-    int dq_n = 0;
-    for (int i = 0; seq.valid(); ++i) {
+    int dqw = 0;                                 // dQ halves this warpgroup has consumed
+    for (int i = wg; seq.valid(); i += NWG) {
       const int tile = seq.tile();
-      TileSeq nseq = seq;
+      TileSeq nseq = seq;                        // the CTA's next tile (ends a run?)
       nseq.next();
+      TileSeq mseq = nseq;                       // this warpgroup's next tile
+#pragma unroll
+      for (int k = 1; k < NWG; ++k) mseq.next();
       const TileDesc ndsc = load_desc(p, nseq);
-      mbar_wait_sticky(&sdp_full, i & 1, p.status, &fail);
+      const TileDesc mdsc = NWG == 1 ? ndsc : load_desc(p, mseq);
+      mbar_wait_sticky(&sdp_full[wg], (i / NWG) & 1, p.status, &fail);
       tc_fence_after();
       // ---- P and dS of this row, written in 16 bits as MMA operands ----
 #pragma unroll
@@ -426,36 +495,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         st_row_chunks<kFp16>(sDS, row, 4, z);
       }
       tc_fence_before();
-      if (!L::kDqAlias) mbar_arrive(&sdp_free);
+      if (!L::kDqAlias) mbar_arrive(&sdp_free[wg]);
       fence_proxy_async_smem();
-      mbar_arrive(&pds_full);
-      // the next tile's row metadata: its loads overlap the MMAs and the epilogue
+      mbar_arrive(&pds_full[wg]);
+      // this warpgroup's next tile's row metadata: its loads overlap the MMAs and the epilogue
       int nlim = -1;
       float nlse2 = 0.f, ndval = 0.f;
-      if (nseq.valid()) row_meta(ndsc, nlim, nlse2, ndval);
+      if (mseq.valid()) row_meta(mdsc, nlim, nlse2, ndval);
 
       // ---- dQ epilogue: TMEM -> 16 bits -> this warp's staging slots -> TMA
-      //      stores.  The slots lie in the P buffer (and, with a single dQ pass,
-      //      the dS buffer too): free once the dQ MMA of this tile completed ----
+      //      stores.  The slots lie in this warpgroup's P buffer (and, with a single
+      //      dQ pass, its dS buffer too): free once the dQ MMA of this tile completed ----
       constexpr int kSlots = (NH == 1 ? 2 : 1) * static_cast<int>(L::kP / (4 * 4096));
       const uint32_t stg = sP + (warp & 3) * kSlots * 4096u;
       int used = 0;                              // stores issued from this warp's slots
 #pragma unroll
       for (int hh = 0; hh < NH; ++hh) {
-        mbar_wait_sticky(&dq_full, dq_n & 1, p.status, &fail);
-        ++dq_n;
+        mbar_wait_sticky(&dq_full[wg], dqw & 1, p.status, &fail);
+        ++dqw;
         tc_fence_after();
 #pragma unroll
         for (int cb = 0; cb < DQC / 64; ++cb) {
           float v[64];
           tmem_ld64(tDQ + lane_off + cb * 64, v);
-          if (hh == NH - 1 && cb == DQC / 64 - 1) {
+          if (cb == DQC / 64 - 1) {
             tc_fence_before();
             mbar_arrive(&dq_free);
-            if (L::kDqAlias) mbar_arrive(&sdp_free);
-          } else if (cb == DQC / 64 - 1) {
-            tc_fence_before();
-            mbar_arrive(&dq_free);
+            if (L::kDqAlias && hh == NH - 1) mbar_arrive(&sdp_free[wg]);
           }
           uint32_t pk[32];
 #pragma unroll
@@ -481,16 +547,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ++used;
         }
       }
-      // the staging slots are the next tile's P/dS rows, written by all four warps:
-      // every warp's stores must have been read first
+      // the staging slots are this warpgroup's next P/dS rows, written by all four of
+      // its warps: every warp's stores must have been read first
       if (lane == 0) bulk_wait_read_all();
-      named_bar_sync(1, 128);
+      named_bar_sync(1 + wg, 128);
 
-      // ---- end of a run of tiles of one block: dK, dV partials out (fp32) ----
-      const bool last = !nseq.valid() || !same_kv(ndsc, dsc);
+      // ---- end of a run: dK, dV partials out (fp32), one slot per (segment, chunk) ----
+      const bool last = !nseq.valid() || !same_run(tile, dsc, nseq.tile(), ndsc);
       if (last) {
         const int seg = p.tseg[tile];
-        const int slot = p.part_off[seg] + static_cast<int>(blockIdx.x) - p.tile_off[seg] / per;
+        const int slot = p.part_off[seg] + tile / C - p.tile_off[seg] / C;
         float *dst = p.dkvbuf + (int64_t)slot * 2 * BK * D;
 #pragma unroll
         for (int hh = 0; hh < NH; ++hh) {
@@ -512,8 +578,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before();
         mbar_arrive(&dkv_free);
       }
-      seq = nseq;
-      dsc = ndsc;
+      seq = mseq;
+      dsc = mdsc;
       lim = nlim;
       lse2 = nlse2;
       dval = ndval;
@@ -571,9 +637,12 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(Params p) {
     *reinterpret_cast<uint32_t *>(dst + e) = pack2<kFp16>(acc[e] * p.scale, acc[e + 1] * p.scale);
 }
 
-// dk, dv of one (KV head, block): sum of the segment's partials (zeros if none).
+// dk, dv of eight keys of one (KV head, block): sums of the segment's partials
+// (zeros if none).  Block (seg, y) takes keys [8 y, 8 y + 8); each thread four
+// consecutive d elements of one key, reading eight partials at a time.
+constexpr int kDkvKeys = 8;
 template <int D, int BK, bool kFp16>
-__global__ void __launch_bounds__(256) bwd_dkv_kernel(Params p) {
+__global__ void __launch_bounds__(kDkvKeys * D / 4) bwd_dkv_kernel(Params p) {
   const int nb = *p.nb;
   const int seg = blockIdx.x;
   if (seg >= p.h_k * nb) return;
@@ -582,21 +651,34 @@ __global__ void __launch_bounds__(256) bwd_dkv_kernel(Params p) {
   const int b = gb - p.blk_start[s];
   const int key0 = p.cu[s] + b * BK;
   const int nkeys = min(BK, p.cu[s + 1] - key0);
+  const int key = blockIdx.y * kDkvKeys + static_cast<int>(threadIdx.x) / (D / 4);
+  const int x = (static_cast<int>(threadIdx.x) % (D / 4)) * 4;
+  if (key >= nkeys) return;
   const int c0 = p.part_off[seg], c1 = p.part_off[seg + 1];
-  uint16_t *dk = static_cast<uint16_t *>(p.dk), *dv = static_cast<uint16_t *>(p.dv);
-  for (int idx = threadIdx.x * 2; idx < nkeys * D; idx += blockDim.x * 2) {
-    const int key = idx / D, x = idx - key * D;
-    float ak0 = 0.f, ak1 = 0.f, av0 = 0.f, av1 = 0.f;
-    for (int c = c0; c < c1; ++c) {
-      const float *src = p.dkvbuf + (int64_t)c * 2 * BK * D;
-      const float2 v2 = *reinterpret_cast<const float2 *>(src + key * D + x);
-      const float2 k2 = *reinterpret_cast<const float2 *>(src + BK * D + key * D + x);
-      av0 += v2.x; av1 += v2.y; ak0 += k2.x; ak1 += k2.y;
+  const float *base = p.dkvbuf + (int64_t)key * D + x;
+  float4 av = make_float4(0.f, 0.f, 0.f, 0.f), ak = av;
+  for (int c = c0; c < c1; c += 8) {
+    float4 v[8], k[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool ok = c + u < c1;
+      const float *src = base + (int64_t)(ok ? c + u : c0) * 2 * BK * D;
+      v[u] = ok ? __ldg(reinterpret_cast<const float4 *>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      k[u] = ok ? __ldg(reinterpret_cast<const float4 *>(src + BK * D))
+                : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const int64_t o = ((int64_t)(key0 + key) * p.h_k + h) * D + x;
-    *reinterpret_cast<uint32_t *>(dk + o) = pack2<kFp16>(ak0 * p.scale, ak1 * p.scale);
-    *reinterpret_cast<uint32_t *>(dv + o) = pack2<kFp16>(av0, av1);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      av.x += v[u].x; av.y += v[u].y; av.z += v[u].z; av.w += v[u].w;
+      ak.x += k[u].x; ak.y += k[u].y; ak.z += k[u].z; ak.w += k[u].w;
+    }
   }
+  uint16_t *dk = static_cast<uint16_t *>(p.dk), *dv = static_cast<uint16_t *>(p.dv);
+  const int64_t o = ((int64_t)(key0 + key) * p.h_k + h) * D + x;
+  *reinterpret_cast<uint2 *>(dk + o) =
+      make_uint2(pack2<kFp16>(ak.x * p.scale, ak.y * p.scale),
+                 pack2<kFp16>(ak.z * p.scale, ak.w * p.scale));
+  *reinterpret_cast<uint2 *>(dv + o) = make_uint2(pack2<kFp16>(av.x, av.y), pack2<kFp16>(av.z, av.w));
 }
 
 // ---------------------------------------------------------------------------
@@ -616,7 +698,7 @@ static cudaError_t run_bwd(const Params &p, int num_sms, int64_t max_tiles, cuda
   int grid = num_sms < kMaxBwdCtas ? num_sms : kMaxBwdCtas;
   mark(7, stream, true);
   bwd_pre_kernel<D, kFp16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
-  bwd_parts_kernel<<<1, 1024, 0, stream>>>(p, grid);
+  bwd_parts_kernel<<<1, 1024, 0, stream>>>(p);
   mark(7, stream, false);
   const uint32_t smem = L::kBytes;
   cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D, BK, kFp16>,
@@ -624,14 +706,16 @@ static cudaError_t run_bwd(const Params &p, int num_sms, int64_t max_tiles, cuda
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   mark(8, stream, true);
-  bwd_main_kernel<D, BK, kFp16><<<static_cast<unsigned>(grid), kBwdThreads, smem, stream>>>(
+  bwd_main_kernel<D, BK, kFp16><<<static_cast<unsigned>(grid), L::kThreads, smem, stream>>>(
       mk, mv, mdq, p);
   mark(8, stream, false);
   mark(9, stream, true);
   bwd_dq_kernel<D, kFp16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
   mark(9, stream, false);
   mark(10, stream, true);
-  bwd_dkv_kernel<D, BK, kFp16><<<static_cast<unsigned>(p.h_k * p.nb_max), 256, 0, stream>>>(p);
+  bwd_dkv_kernel<D, BK, kFp16>
+      <<<dim3(static_cast<unsigned>(p.h_k * p.nb_max), BK / kDkvKeys), kDkvKeys * D / 4, 0,
+         stream>>>(p);
   mark(10, stream, false);
   return cudaGetLastError();
 }

@@ -83,6 +83,7 @@ struct Params {
   int64_t nb_max, n_idx_tiles, nsub, n_scan_ctas;
   int idx_tok, n_w, wave_tiles;
   int fwd_chunk;    // forward schedule: consecutive tiles per chunk, chunks dealt round-robin
+  int bwd_chunk;    // the same for the backward main kernel
   void *obuf;       // forward partial outputs [tiles * 128, d] (dtype), tile-padded rows
   float2 *mlbuf;    // forward partial (max, sum) per padded row, log2 domain
   float *dstat;     // backward D = rowsum(dO * O) [h_q, N]
@@ -160,6 +161,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking probe of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
       : "r"(addr), "r"(parity)

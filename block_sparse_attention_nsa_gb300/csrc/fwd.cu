@@ -66,8 +66,8 @@ constexpr int kFwdThreads = 512;
 //     Q rows of tiles w, w + NPW, ... by
 //     cp.async (16-byte chunks, a warp instruction covering 256 / d whole rows,
 //     so reads are fully coalesced) into the 128-byte-swizzled operand layout,
-//     waits for its own copies and arrives; a Q stage is released as soon as the
-//     S MMA that reads it completes;
+//     waits for its own copies and arrives; a Q stage is released (by the softmax
+//     warpgroup of its tile) as soon as the S MMA that reads it has completed;
 //   warp 6 (one thread): K_b and V_b by TMA (3-D tensor maps, once per change of
 //     (KV head, block));
 //   warp 4 (one thread): tcgen05 MMAs S(i) = Q K^T into TMEM slot i % 2 and
@@ -257,22 +257,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         lo_k[j] = sdesc_lo_sw128(sK0 + j * L::kK, 16);
         lo_v[j] = sdesc_lo_sw128(sV0 + j * L::kK, BK * 128);
       }
-      uint32_t flags[2] = {0u, 0u};   // K/V flags of tiles i and i + 1 (index i & 1)
-      int kvs[2] = {0, 0};            // K/V stage of tiles i and i + 1
+      // K/V flags and K/V stage of the even (a) and odd (b) tile in flight, kept in
+      // registers (no dynamically indexed arrays in the issue loop)
+      uint32_t fl_a = 0u, fl_b = 0u;
+      int ks_a = 0, ks_b = 0;
       int s_next = 0;                 // next tile whose S has to be issued
       int s_kv = 0;                   // K/V loads consumed so far (load m fills stage m % KVS)
       auto issue_s = [&]() {
         const int i = s_next, qs = i % QS;
         mbar_wait_sticky(&q_full[qs], (i / QS) & 1, p.status, &fail);
         const uint32_t f = q_flags[qs];
-        flags[i & 1] = f;
         if (f & 0x100u) {
           // load s_kv is the (s_kv / KVS)-th fill of stage s_kv % KVS
           mbar_wait_sticky(&kv_full[s_kv % KVS], (s_kv / KVS) & 1, p.status, &fail);
           ++s_kv;
         }
         const int ks = (s_kv - 1) % KVS;
-        kvs[i & 1] = ks;
+        if (i & 1) {
+          fl_b = f;
+          ks_b = ks;
+        } else {
+          fl_a = f;
+          ks_a = ks;
+        }
         tc_fence_after();
         uint32_t aq = lo_q[0], bk = lo_k[0];
 #pragma unroll
@@ -284,8 +291,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk)
           mma_f16(tSd, sdesc_join(aq + (kmajor_step(128, kk) >> 4), kHiK),
                   sdesc_join(bk + (kmajor_step(BK, kk) >> 4), kHiK), kIdescS, kk > 0);
-        mma_commit(&s_full[i & 1]);
-        mma_commit(&q_empty[qs]);
+        mma_commit(&s_full[i & 1]);   // the softmax warpgroup then releases Q stage qs
         ++s_next;
       };
       for (int i = 0; i < n; ++i) {
@@ -293,11 +299,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // S(i + 1) goes ahead of O(i) when its Q rows are already in and its K/V
         // stage is not one that only O(i) releases (a single K/V stage and a
         // change of block after tile i)
-        if (s_next == i + 1 && i + 1 < n && !(KVS == 1 && (flags[i & 1] & 0x200u)) &&
-            mbar_try_wait(smem_u32(&q_full[(i + 1) % QS]), ((i + 1) / QS) & 1))
+        const uint32_t f = (i & 1) ? fl_b : fl_a;
+        if (s_next == i + 1 && i + 1 < n && !(KVS == 1 && (f & 0x200u)) &&
+            mbar_test_wait(smem_u32(&q_full[(i + 1) % QS]), ((i + 1) / QS) & 1))
           issue_s();
-        const uint32_t f = flags[i & 1];
-        const int ks = kvs[i & 1], os = i % OS;
+        const int ks = (i & 1) ? ks_b : ks_a, os = i % OS;
         mbar_wait_sticky(&p_full[i & 1], (i >> 1) & 1, p.status, &fail);
         if (i >= OS) mbar_wait_sticky(&o_free[os], ((i / OS) - 1) & 1, p.status, &fail);
         tc_fence_after();
@@ -344,6 +350,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const bool row_in = row < nrows;
       const int os = i % OS;
       mbar_wait_sticky(&s_full[i & 1], (i >> 1) & 1, p.status, &fail);
+      // S(i) is complete, so its MMAs have read Q stage i % QS: release it
+      if (row == 0) mbar_arrive(&q_empty[i % QS]);
       tc_fence_after();
       const uint32_t tS = tS0 + (i & 1) * BK + lane_off;
       float lsum = 0.f, m2 = 0.f;
