@@ -43,6 +43,9 @@ struct FwdSmem {
                        OS = fwd_os(D, BK);
   static constexpr int NPW = QS < 4 ? QS : 4;   // Q producer warps (one per stage or more)
   static_assert(QS % NPW == 0, "each Q stage needs a single producer warp");
+  // each of the two MMA threads consumes every other tile: with an even number of Q
+  // stages each stage belongs to one thread; a single stage is handled explicitly
+  static_assert(QS % 2 == 0 || QS == 1, "Q stages: even, or one");
   static constexpr uint32_t kQ = 128u * D * 2u;            // one Q stage
   static constexpr uint32_t kK = uint32_t(BK) * D * 2u;     // one K (or V) stage
   static constexpr uint32_t kStg = 128u * 64u * 2u;         // staging of one warpgroup
@@ -57,8 +60,8 @@ struct FwdSmem {
   static constexpr uint32_t kTmemCols = 512;
 };
 
-// warps 0-3 Q producers, warp 4 MMA, warp 5 TMEM owner, warp 6 K/V producer,
-// warps 8-11 / 12-15 two softmax WGs
+// warps 0-3 Q producers, warps 4 and 7 MMA issuers, warp 5 TMEM owner, warp 6 K/V
+// producer, warps 8-11 / 12-15 two softmax WGs
 constexpr int kFwdThreads = 512;
 
 // Persistent, warp-specialised forward main kernel (one CTA per SM).
@@ -70,8 +73,9 @@ constexpr int kFwdThreads = 512;
 //     warpgroup of its tile) as soon as the S MMA that reads it has completed;
 //   warp 6 (one thread): K_b and V_b by TMA (3-D tensor maps, once per change of
 //     (KV head, block));
-//   warp 4 (one thread): tcgen05 MMAs S(i) = Q K^T into TMEM slot i % 2 and
-//     O(i) = P V into an O accumulator, issued as S(0), S(1), O(0), S(2), O(1), ...;
+//   warps 4 and 7 (one thread each): tcgen05 MMAs of the even and of the odd
+//     tiles, S(i) = Q K^T into TMEM slot i % 2 and O(i) = P V into an O
+//     accumulator, issued as S(i), O(i), S(i + 2), ... by each;
 //   warps 8-11 / 12-15: softmax of even / odd tiles (row max, exp2, P in 16 bits
 //     back to TMEM, fp32 row sum) and their epilogue (O from TMEM to 16 bits,
 //     staged one 64-column block at a time and written by TMA tensor stores to
@@ -92,10 +96,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t q_full[QS], q_empty[QS], kv_full[KVS], kv_empty[KVS], s_full[2],
       p_full[2], o_full[2], o_free[OS];
-  // Per Q stage: K/V flags of the stage's tile, written by the producer before it
-  // arms q_full and read by the MMA thread after q_full completes:
-  //   bits 0-7 K/V stage, bit 8 first tile of that K/V, bit 9 last tile of it.
-  __shared__ uint32_t q_flags[QS];
   __shared__ uint32_t tmem_base;
   __shared__ int fail;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -107,7 +107,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 5) tmem_alloc(&tmem_base, L::kTmemCols);
   if (tid == 0) {
     for (int i = 0; i < QS; ++i) { mbar_init(&q_full[i], 32); mbar_init(&q_empty[i], 1); }
-    for (int i = 0; i < KVS; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
+    // kv_empty: one arrival from each MMA thread
+    for (int i = 0; i < KVS; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 2); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
@@ -152,26 +153,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
     };
-    auto same_kv = [](const TileDesc &a, const TileDesc &b) {
-      return (a.hn & 0xffff) == (b.hn & 0xffff) && a.key0 == b.key0;
-    };
     const uint16_t *gq = static_cast<const uint16_t *>(p.q);
     const uint64_t keep = l2_evict_last();    // Q rows are gathered ~T times each
     int li = warp;
-    // prv = the tile before this warp's current one in the CTA's sequence
-    TileSeq prv;
-    prv.init(total, p.fwd_chunk);
-    for (int k = 0; k + 1 < warp; ++k) prv.next();
     while (seq.valid()) {
       const TileDesc dc = load_desc(p, seq);
-      TileSeq sn = seq;
-      sn.next();
-      const TileDesc dn = load_desc(p, sn);
-      const TileDesc dp = li > 0 ? load_desc(p, prv) : TileDesc{0, 0, -1, -1};
       int rid[4];
       tile_rids(dc, rid);
-      const bool first = li == 0 || !same_kv(dp, dc);
-      const bool last = !sn.valid() || !same_kv(dn, dc);
       const int qs = li % QS;
       if (li >= QS) mbar_wait_sticky(&q_empty[qs], ((li / QS) - 1) & 1, p.status, &fail);
       const uint32_t stage = sQ0 + qs * L::kQ;
@@ -188,16 +176,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
       cp_async_commit();
-      if (lane == 0) q_flags[qs] = (first ? 0x100u : 0u) | (last ? 0x200u : 0u);
       cp_async_wait_all();
       fence_proxy_async_smem();
       mbar_arrive(&q_full[qs]);
-      // next tile of this warp: li + NPW; its predecessor is li + NPW - 1
-      prv = seq;
 #pragma unroll
-      for (int k = 0; k + 1 < NPW; ++k) prv.next();
-      seq = prv;
-      seq.next();
+      for (int k = 0; k < NPW; ++k) seq.next();   // this warp's next tile: li + NPW
       li += NPW;
     }
   } else if (warp == 6) {
@@ -240,84 +223,102 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         dn = dnn;
       }
     }
-  } else if (warp == 4) {
-    // ------------------------------ MMA issuer ------------------------------
-    if (lane == 0) {
-      TileSeq seq;
-      seq.init(total, p.fwd_chunk);
-      int n = 0;    // tiles of this CTA
-      for (TileSeq c = seq; c.valid(); c.next()) ++n;
-      // descriptor words: constant upper words, per-stage lower words
-      constexpr uint32_t kHiK = sdesc_hi_sw128(1024);   // K-major Q, K and MN-major V
-      uint32_t lo_q[QS], lo_k[KVS], lo_v[KVS];
+  } else if ((warp == 4 || warp == 7) && lane == 0) {
+    // ------------------------------ MMA issuers ------------------------------
+    // Thread w (warp 4 for w = 0, warp 7 for w = 1) issues the MMAs of the tiles of
+    // softmax warpgroup w, i = w, w + 2, ...: S(i) into S slot w, then, once P(i) is
+    // in, O(i); S(i + 2) follows O(i) in the same thread, so the tensor pipe
+    // executes them in order (S(i + 2) overwrites the columns P(i) was read from).
+    // The two threads' MMAs interleave on the tensor pipe, and one thread's waits
+    // for its warpgroup are covered by the other's issue.  Both walk every tile of
+    // the CTA to follow the K/V loads; a load is released (kv_empty, count 2) by
+    // each thread after its last MMA that reads it, or at once if it has none.
+    const int w = warp == 4 ? 0 : 1;
+    constexpr uint32_t kHiK = sdesc_hi_sw128(1024);   // K-major Q, K and MN-major V
+    uint32_t lo_q[QS], lo_k[KVS], lo_v[KVS];
 #pragma unroll
-      for (int j = 0; j < QS; ++j) lo_q[j] = sdesc_lo_sw128(sQ0 + j * L::kQ, 16);
+    for (int j = 0; j < QS; ++j) lo_q[j] = sdesc_lo_sw128(sQ0 + j * L::kQ, 16);
 #pragma unroll
-      for (int j = 0; j < KVS; ++j) {
-        lo_k[j] = sdesc_lo_sw128(sK0 + j * L::kK, 16);
-        lo_v[j] = sdesc_lo_sw128(sV0 + j * L::kK, BK * 128);
+    for (int j = 0; j < KVS; ++j) {
+      lo_k[j] = sdesc_lo_sw128(sK0 + j * L::kK, 16);
+      lo_v[j] = sdesc_lo_sw128(sV0 + j * L::kK, BK * 128);
+    }
+    const uint32_t tSw = tS0 + w * BK;
+    // descriptors of tiles i, i + 1 and i + 2 (loaded two tiles ahead)
+    TileSeq seq;
+    seq.init(total, p.fwd_chunk);
+    TileSeq s2 = seq;
+    s2.next();
+    TileDesc dc = load_desc(p, seq);
+    TileDesc dn = load_desc(p, s2);
+    s2.next();
+    TileDesc dnn = load_desc(p, s2);
+    int m = -1;              // K/V load of the current run (load m fills stage m % KVS)
+    bool own = false;        // this thread has issued an MMA that reads load m
+    int prev_h = -1, prev_key0 = -1;
+    for (int i = 0; seq.valid(); ++i) {
+      const int h = dc.hn & 0xffff;
+      if (h != prev_h || dc.key0 != prev_key0) {   // a new K/V load
+        ++m;
+        own = false;
+        prev_h = h;
+        prev_key0 = dc.key0;
       }
-      // K/V flags and K/V stage of the even (a) and odd (b) tile in flight, kept in
-      // registers (no dynamically indexed arrays in the issue loop)
-      uint32_t fl_a = 0u, fl_b = 0u;
-      int ks_a = 0, ks_b = 0;
-      int s_next = 0;                 // next tile whose S has to be issued
-      int s_kv = 0;                   // K/V loads consumed so far (load m fills stage m % KVS)
-      auto issue_s = [&]() {
-        const int i = s_next, qs = i % QS;
+      TileSeq s1 = seq;
+      s1.next();
+      const bool last = !s1.valid() || (dn.hn & 0xffff) != h || dn.key0 != dc.key0;
+      const int ks = m % KVS;
+      const uint32_t kv_par = (m / KVS) & 1;
+      if ((i & 1) == w) {
+        if (!own) {
+          mbar_wait_sticky(&kv_full[ks], kv_par, p.status, &fail);
+          own = true;
+        }
+        const int qs = i % QS, os = i % OS;
+        if constexpr (QS == 1) {
+          // A single Q stage alternates between the two threads: wait until the other
+          // thread's tile i - 1 has consumed its fill, so that the wait below cannot
+          // be met by the phase of tile i - 2
+          if (i >= 1) mbar_wait_sticky(&s_full[1 - w], ((i - 1) >> 1) & 1, p.status, &fail);
+        }
         mbar_wait_sticky(&q_full[qs], (i / QS) & 1, p.status, &fail);
-        const uint32_t f = q_flags[qs];
-        if (f & 0x100u) {
-          // load s_kv is the (s_kv / KVS)-th fill of stage s_kv % KVS
-          mbar_wait_sticky(&kv_full[s_kv % KVS], (s_kv / KVS) & 1, p.status, &fail);
-          ++s_kv;
-        }
-        const int ks = (s_kv - 1) % KVS;
-        if (i & 1) {
-          fl_b = f;
-          ks_b = ks;
-        } else {
-          fl_a = f;
-          ks_a = ks;
-        }
         tc_fence_after();
-        uint32_t aq = lo_q[0], bk = lo_k[0];
+        uint32_t aq = lo_q[0], bk = lo_k[0], bv = lo_v[0];
 #pragma unroll
         for (int j = 1; j < QS; ++j) aq = qs == j ? lo_q[j] : aq;
 #pragma unroll
-        for (int j = 1; j < KVS; ++j) bk = ks == j ? lo_k[j] : bk;
-        const uint32_t tSd = tS0 + (i & 1) * BK;
+        for (int j = 1; j < KVS; ++j) {
+          bk = ks == j ? lo_k[j] : bk;
+          bv = ks == j ? lo_v[j] : bv;
+        }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_f16(tSd, sdesc_join(aq + (kmajor_step(128, kk) >> 4), kHiK),
+          mma_f16(tSw, sdesc_join(aq + (kmajor_step(128, kk) >> 4), kHiK),
                   sdesc_join(bk + (kmajor_step(BK, kk) >> 4), kHiK), kIdescS, kk > 0);
-        mma_commit(&s_full[i & 1]);   // the softmax warpgroup then releases Q stage qs
-        ++s_next;
-      };
-      for (int i = 0; i < n; ++i) {
-        if (s_next == i) issue_s();
-        // S(i + 1) goes ahead of O(i) when its Q rows are already in and its K/V
-        // stage is not one that only O(i) releases (a single K/V stage and a
-        // change of block after tile i)
-        const uint32_t f = (i & 1) ? fl_b : fl_a;
-        if (s_next == i + 1 && i + 1 < n && !(KVS == 1 && (f & 0x200u)) &&
-            mbar_test_wait(smem_u32(&q_full[(i + 1) % QS]), ((i + 1) / QS) & 1))
-          issue_s();
-        const int ks = (i & 1) ? ks_b : ks_a, os = i % OS;
-        mbar_wait_sticky(&p_full[i & 1], (i >> 1) & 1, p.status, &fail);
+        mma_commit(&s_full[w]);   // the softmax warpgroup then releases Q stage qs
+        mbar_wait_sticky(&p_full[w], (i >> 1) & 1, p.status, &fail);
         if (i >= OS) mbar_wait_sticky(&o_free[os], ((i / OS) - 1) & 1, p.status, &fail);
         tc_fence_after();
-        const uint32_t tP = tS0 + (i & 1) * BK, tOd = tO0 + os * D;
-        uint32_t bv = lo_v[0];
-#pragma unroll
-        for (int j = 1; j < KVS; ++j) bv = ks == j ? lo_v[j] : bv;
+        const uint32_t tOd = tO0 + os * D;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          mma_f16_ts(tOd, tP + kk * 8, sdesc_join(bv + (mnmajor_step(kk) >> 4), kHiK), kIdescO,
-                     kk > 0);
-        mma_commit(&o_full[i & 1]);
-        if (f & 0x200u) mma_commit(&kv_empty[ks]);
+          mma_f16_ts(tOd, tSw + kk * 8, sdesc_join(bv + (mnmajor_step(kk) >> 4), kHiK),
+                     kIdescO, kk > 0);
+        mma_commit(&o_full[w]);
       }
+      if (last) {
+        if (own) {
+          mma_commit(&kv_empty[ks]);
+        } else {
+          mbar_wait_sticky(&kv_full[ks], kv_par, p.status, &fail);
+          mbar_arrive(&kv_empty[ks]);
+        }
+      }
+      seq = s1;
+      dc = dn;
+      dn = dnn;
+      s2.next();
+      dnn = load_desc(p, s2);
     }
   } else if (warp >= 8) {
     // ------------------------- softmax + epilogue -------------------------
