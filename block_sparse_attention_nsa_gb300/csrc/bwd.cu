@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(Params p) {
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  constexpr int kBatch = 8;
+  constexpr int kBatch = 16;   // partial rows in flight per lane
   for (int k0 = 0; k0 < p.topk; k0 += kBatch) {
     uint32_t u[kBatch][E / 2];
 #pragma unroll
@@ -618,9 +618,16 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(Params p) {
       const int64_t r = __shfl_sync(0xffffffffu, row, (k0 + b) & 31);
       const bool ok = k0 + b < p.topk && r >= 0;
       const uint16_t *src = buf + (ok ? r : 0) * D + lane * E;
-#pragma unroll
-      for (int e = 0; e < E / 2; ++e)
-        u[b][e] = ok ? *reinterpret_cast<const uint32_t *>(src + 2 * e) : 0u;
+      if constexpr (E == 2) {
+        u[b][0] = ok ? __ldcs(reinterpret_cast<const unsigned int *>(src)) : 0u;
+      } else if constexpr (E == 4) {
+        const uint2 x = ok ? __ldcs(reinterpret_cast<const uint2 *>(src)) : make_uint2(0u, 0u);
+        u[b][0] = x.x; u[b][1] = x.y;
+      } else {
+        const uint4 x = ok ? __ldcs(reinterpret_cast<const uint4 *>(src))
+                           : make_uint4(0u, 0u, 0u, 0u);
+        u[b][0] = x.x; u[b][1] = x.y; u[b][2] = x.z; u[b][3] = x.w;
+      }
     }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b)

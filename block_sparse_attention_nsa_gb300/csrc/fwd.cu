@@ -510,6 +510,30 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(Params p) {
     const int32_t pr = p.prow[((int64_t)h * p.n + t) * p.topk + lane];
     if (pr >= 0) row = (int64_t)pr + j;
   }
+  // The partial rows are loaded first, sixteen at a time, so that their latency
+  // overlaps the (m, l) load and the reductions of the weights.
+  constexpr int kBatch = 16;
+  const uint16_t *obuf = static_cast<const uint16_t *>(p.obuf);
+  auto load_rows = [&](int k0, uint32_t (&u)[kBatch][E / 2]) {
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t r = __shfl_sync(0xffffffffu, row, (k0 + b) & 31);
+      const bool ok = k0 + b < p.topk && r >= 0;
+      const uint16_t *src = obuf + (ok ? r : 0) * D + lane * E;
+      if constexpr (E == 2) {
+        u[b][0] = ok ? __ldcs(reinterpret_cast<const unsigned int *>(src)) : 0u;
+      } else if constexpr (E == 4) {
+        const uint2 x = ok ? __ldcs(reinterpret_cast<const uint2 *>(src)) : make_uint2(0u, 0u);
+        u[b][0] = x.x; u[b][1] = x.y;
+      } else {
+        const uint4 x = ok ? __ldcs(reinterpret_cast<const uint4 *>(src))
+                           : make_uint4(0u, 0u, 0u, 0u);
+        u[b][0] = x.x; u[b][1] = x.y; u[b][2] = x.z; u[b][3] = x.w;
+      }
+    }
+  };
+  uint32_t u[kBatch][E / 2];
+  load_rows(0, u);
   float2 ml = make_float2(-INFINITY, 0.f);
   if (row >= 0) ml = p.mlbuf[row];
   float M = ml.x;
@@ -523,37 +547,18 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(Params p) {
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  const uint16_t *obuf = static_cast<const uint16_t *>(p.obuf);
-  // eight partial rows in flight per lane before any is consumed
-  constexpr int kBatch = 8;
   for (int k0 = 0; k0 < p.topk; k0 += kBatch) {
-    uint32_t u[kBatch][E / 2];
-    float wk[kBatch];
+    if (k0 > 0) load_rows(k0, u);
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
-      const int64_t r = __shfl_sync(0xffffffffu, row, (k0 + b) & 31);
-      wk[b] = __shfl_sync(0xffffffffu, w, (k0 + b) & 31);
-      const bool ok = k0 + b < p.topk && r >= 0;
-      if (!ok) wk[b] = 0.f;
-      const uint16_t *src = obuf + (ok ? r : 0) * D + lane * E;
-      if constexpr (E == 2) {
-        u[b][0] = ok ? *reinterpret_cast<const uint32_t *>(src) : 0u;
-      } else if constexpr (E == 4) {
-        const uint2 x = ok ? *reinterpret_cast<const uint2 *>(src) : make_uint2(0u, 0u);
-        u[b][0] = x.x; u[b][1] = x.y;
-      } else {
-        const uint4 x = ok ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0u, 0u, 0u, 0u);
-        u[b][0] = x.x; u[b][1] = x.y; u[b][2] = x.z; u[b][3] = x.w;
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b)
+      const float wk = __shfl_sync(0xffffffffu, w, (k0 + b) & 31);   // 0 for empty slots
 #pragma unroll
       for (int e = 0; e < E / 2; ++e) {
         const float2 f = unpack2<kFp16>(u[b][e]);
-        acc[2 * e] = fmaf(wk[b], f.x, acc[2 * e]);
-        acc[2 * e + 1] = fmaf(wk[b], f.y, acc[2 * e + 1]);
+        acc[2 * e] = fmaf(wk, f.x, acc[2 * e]);
+        acc[2 * e + 1] = fmaf(wk, f.y, acc[2 * e + 1]);
       }
+    }
   }
   const bool any = lsum > 0.f;
   const float inv = any ? 1.f / lsum : 0.f;
