@@ -29,6 +29,31 @@ sys.path.insert(0, ROOT)
 METRIC = "selected-attn fwd/bwd ms & useful TFLOP/s (% BF16 tensor peak) at 64K, B_K=64, T=16"
 DOMINANT = ("fwd_main", "bwd_main")
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
+# kernels on the 64K workload, from one ncu capture of the kernel sources whose
+# SHA-256 is given (profiles/dram_traffic_fwd64k_g4.md).  Reported only while the
+# sources are unchanged; otherwise the roofline's traffic is null.
+TRAFFIC = {"sources_sha256": "8396e0b670b0ed4f44a6e3d00ee14924a6579ffaf73e6aefb6da326a758f100a",
+           "bytes": {"fwd_main": {"4": 925940224 + 4403137280},
+                     "bwd_main": {"4": 2769964800 + 5059977472}}}
+
+
+def kernel_sources_hash() -> str:
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_sparse_attention_nsa_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def captured_traffic(kernel: str, g: int):
+    if not TRAFFIC["sources_sha256"] or TRAFFIC["sources_sha256"] != kernel_sources_hash():
+        return None
+    return TRAFFIC["bytes"].get(kernel, {}).get(str(g))
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -202,10 +227,12 @@ def e2e_measure(r: Runner, iters: int):
     d2h = sum(host[x].numel() * host[x].element_size() for x in ("out", "lse", "dq", "dk", "dv"))
     nsa.step_host(r.dims, host, r.cfg.scale, staging, r.ws)     # warm-up
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
+    times = []
     for _ in range(iters):
-        nsa.step_host(r.dims, host, r.cfg.scale, staging, r.ws)
-    dt = (time.perf_counter() - t0) / iters
+        t0 = time.perf_counter()
+        nsa.step_host(r.dims, host, r.cfg.scale, staging, r.ws)  # returns after the D2H copies
+        times.append(time.perf_counter() - t0)
+    dt = float(np.median(times))
     del staging
     return dt, h2d, d2h
 
@@ -324,7 +351,8 @@ def run_ours(args, rank, world):
         "kernels_ms_per_step": {k: t / prof_steps for k, (n, t) in kern.items() if n},
         "kernels_sum_ms_per_step": step_tot / prof_steps,
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": pk_burst,
-                     "unit": "TFLOP/s", "frac": achieved / pk_burst, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / pk_burst,
+                     "traffic": captured_traffic(dom, cfg.g),
                      "peak_kind": f"{pk_kind} bf16 burst",
                      "share_of_step": tot / step_tot if step_tot else None,
                      "algorithmic_flops_per_launch": dom_flops},
@@ -332,7 +360,7 @@ def run_ours(args, rank, world):
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_e2e:
-        dt, h2d, d2h = e2e_measure(r, 3)
+        dt, h2d, d2h = e2e_measure(r, 5)
         result["e2e"] = {"value": step_flops / dt / 1e12, "unit": "TFLOP/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "ms_per_step": dt * 1e3}

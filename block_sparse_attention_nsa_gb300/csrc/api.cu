@@ -2,6 +2,7 @@
 // layout, kernel launches and the optional per-kernel event timing.
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "common.cuh"
@@ -400,6 +401,37 @@ nsa_status nsa_sel_attn_staging_size(const nsa_sel_attn_dims *dims, size_t *byte
   return NSA_OK;
 }
 
+// Side stream and events of nsa_sel_attn_step_host, one set per device, created on
+// first use and kept for the life of the process.
+struct StepAux {
+  int device = -1;
+  cudaStream_t side = nullptr;
+  cudaEvent_t dout_in = nullptr, fwd_done = nullptr, out_back = nullptr;
+};
+static bool step_aux(StepAux **aux) {
+  static std::mutex mu;
+  static std::vector<StepAux> all;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto &a : all)
+    if (a.device == dev) {
+      *aux = &a;
+      return true;
+    }
+  StepAux a;
+  a.device = dev;
+  if (cudaStreamCreateWithFlags(&a.side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&a.dout_in, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&a.fwd_done, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&a.out_back, cudaEventDisableTiming) != cudaSuccess)
+    return false;
+  all.reserve(16);
+  all.push_back(a);
+  *aux = &all.back();
+  return true;
+}
+
 nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const void *host_q,
                                   const void *host_k, const void *host_v,
                                   const int32_t *host_sel_idx, const int32_t *host_cu_seqlens,
@@ -431,9 +463,20 @@ nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const void *hos
   char *sel = take(selbytes), *cu = take(cubytes), *out = take(qbytes);
   char *lse = take(lsebytes), *dq = take(qbytes), *dk = take(kbytes), *dv = take(kbytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  StepAux *aux = nullptr;
+  if (!step_aux(&aux)) return NSA_ERR_CUDA;
+  cudaStream_t s2 = aux->side;
+  // dout travels on the side stream while the forward runs; out and lse travel back
+  // on it while the backward runs
+  if (cudaEventRecord(aux->fwd_done, s) != cudaSuccess ||            // s2 after s's earlier work
+      cudaStreamWaitEvent(s2, aux->fwd_done, 0) != cudaSuccess)
+    return NSA_ERR_CUDA;
+  if (qbytes && cudaMemcpyAsync(dout, host_dout, qbytes, cudaMemcpyHostToDevice, s2) != cudaSuccess)
+    return NSA_ERR_CUDA;
+  if (cudaEventRecord(aux->dout_in, s2) != cudaSuccess) return NSA_ERR_CUDA;
   const struct { void *dst; const void *src; size_t n; } h2d[] = {
-      {q, host_q, qbytes}, {k, host_k, kbytes}, {v, host_v, kbytes}, {dout, host_dout, qbytes},
-      {sel, host_sel_idx, selbytes}, {cu, host_cu_seqlens, cubytes}};
+      {sel, host_sel_idx, selbytes}, {cu, host_cu_seqlens, cubytes}, {q, host_q, qbytes},
+      {k, host_k, kbytes}, {v, host_v, kbytes}};
   for (const auto &c : h2d)
     if (c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s) != cudaSuccess)
       return NSA_ERR_CUDA;
@@ -441,16 +484,27 @@ nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const void *hos
                         reinterpret_cast<int32_t *>(cu), scale, out, reinterpret_cast<float *>(lse),
                         workspace, workspace_bytes, stream);
   if (st != NSA_OK) return st;
+  if (cudaEventRecord(aux->fwd_done, s) != cudaSuccess ||
+      cudaStreamWaitEvent(s2, aux->fwd_done, 0) != cudaSuccess)
+    return NSA_ERR_CUDA;
+  const struct { void *dst; const void *src; size_t n; } back1[] = {
+      {host_out, out, qbytes}, {host_lse, lse, host_lse ? lsebytes : 0}};
+  for (const auto &c : back1)
+    if (c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToHost, s2) != cudaSuccess)
+      return NSA_ERR_CUDA;
+  if (cudaEventRecord(aux->out_back, s2) != cudaSuccess ||
+      cudaStreamWaitEvent(s, aux->dout_in, 0) != cudaSuccess)
+    return NSA_ERR_CUDA;
   st = nsa_sel_attn_bwd(dims, q, k, v, reinterpret_cast<int32_t *>(sel),
                         reinterpret_cast<int32_t *>(cu), scale, out, reinterpret_cast<float *>(lse),
                         dout, dq, dk, dv, workspace, workspace_bytes, 1, stream);
   if (st != NSA_OK) return st;
-  const struct { void *dst; const void *src; size_t n; } d2h[] = {
-      {host_out, out, qbytes}, {host_lse, lse, host_lse ? lsebytes : 0}, {host_dq, dq, qbytes},
-      {host_dk, dk, kbytes}, {host_dv, dv, kbytes}};
-  for (const auto &c : d2h)
+  const struct { void *dst; const void *src; size_t n; } back2[] = {
+      {host_dq, dq, qbytes}, {host_dk, dk, kbytes}, {host_dv, dv, kbytes}};
+  for (const auto &c : back2)
     if (c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToHost, s) != cudaSuccess)
       return NSA_ERR_CUDA;
+  if (cudaStreamWaitEvent(s, aux->out_back, 0) != cudaSuccess) return NSA_ERR_CUDA;
   return cuda_status(cudaStreamSynchronize(s));
 }
 

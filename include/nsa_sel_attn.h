@@ -139,8 +139,11 @@ NSA_API nsa_status nsa_sel_attn_staging_size(const nsa_sel_attn_dims *dims, size
 /* One training step of the branch from HOST buffers: copies q, k, v, dout,
  * sel_idx and cu_seqlens to the caller's device staging buffer, runs forward and
  * backward (reusing the index), copies out, lse, dq, dk and dv back to the host
- * buffers, and synchronises the stream.  Host buffers should be pinned for the
- * copies to be asynchronous.  host_lse may be NULL to skip that copy. */
+ * buffers, and synchronises the stream.  dout is uploaded, and out and lse are
+ * downloaded, on a side stream that the library creates once per device, so those
+ * copies overlap the forward and the backward; the call returns only after every
+ * copy of both streams is complete.  Host buffers should be pinned for the copies
+ * to be asynchronous.  host_lse may be NULL to skip that copy. */
 NSA_API nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const void *host_q,
                                   const void *host_k, const void *host_v,
                                   const int32_t *host_sel_idx, const int32_t *host_cu_seqlens,
