@@ -127,12 +127,10 @@ nsa_status make_layout(const nsa_sel_attn_dims *d, Layout *L) {
   L->max_pairs = h_k * N * T;
   L->max_rows = L->max_pairs * g;
   L->max_tiles = (L->max_rows + kTileRows - 1) / kTileRows + h_k * L->nb_max;
-  L->max_chunks = (L->max_tiles + kBwdChunkTiles - 1) / kBwdChunkTiles + h_k * L->nb_max;
   if (L->nb_max * 4 > kIdxSmemCap) return NSA_ERR_UNSUPPORTED;
-  // scatter: token masks (1 bit), warp prefixes (1 byte) and two bases per block,
-  // plus the tile's slot_map and prow rows
+  // scatter: token masks (1 bit), warp prefixes (1 byte) and two bases per block
   auto scatter_bytes = [&](int tok) {
-    return (tok / 32) * L->nb_max * 5 + 2 * L->nb_max * 4 + 2 * (int64_t)tok * T * 4 + 16;
+    return (tok / 32) * L->nb_max * 5 + 2 * L->nb_max * 4 + 16;
   };
   int tok = kIdxThreads;
   while (tok > 32 && scatter_bytes(tok) > kIdxSmemCap) tok >>= 1;
@@ -164,7 +162,6 @@ nsa_status make_layout(const nsa_sel_attn_dims *d, Layout *L) {
   L->counts = take(4 * nseg1);
   L->offsets = take(4 * nseg1);
   L->tile_off = take(4 * nseg1);
-  L->chunk_off = take(4 * nseg1);
   L->q_list = take(4 * static_cast<size_t>(L->max_pairs > 0 ? L->max_pairs : 1));
   L->slot_map = take(4 * hnt);
   L->chunk_hist = take(4 * static_cast<size_t>(h_k * L->n_idx_tiles * L->nb_max));
@@ -210,7 +207,6 @@ void fill_params(Params *p, const nsa_sel_attn_dims *d, const Layout &L, void *w
   p->counts = reinterpret_cast<int32_t *>(w + L.counts);
   p->offsets = reinterpret_cast<int32_t *>(w + L.offsets);
   p->tile_off = reinterpret_cast<int32_t *>(w + L.tile_off);
-  p->chunk_off = reinterpret_cast<int32_t *>(w + L.chunk_off);
   p->q_list = reinterpret_cast<int32_t *>(w + L.q_list);
   p->slot_map = reinterpret_cast<int32_t *>(w + L.slot_map);
   p->chunk_hist = reinterpret_cast<int32_t *>(w + L.chunk_hist);

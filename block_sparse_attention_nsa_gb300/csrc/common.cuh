@@ -17,7 +17,6 @@ namespace nsa {
 // Tiling constants
 // ---------------------------------------------------------------------------
 constexpr int kTileRows = 128;      // gathered (token, query head) rows per MMA tile (tcgen05 M)
-constexpr int kBwdChunkTiles = 8;   // backward: row tiles one CTA accumulates dK/dV over
 constexpr int kIdxThreads = 256;    // index builder: threads per CTA (one token per thread)
 constexpr int kThreads = 128;       // backward main kernel: one thread per tile row / TMEM lane
 constexpr int kScanPer = 4096;      // entries per CTA of the multi-CTA exclusive scan
@@ -31,7 +30,6 @@ struct Layout {
   int64_t max_pairs;       // upper bound on kept (token, slot) pairs: h_k * N * T
   int64_t max_rows;        // max_pairs * g
   int64_t max_tiles;       // upper bound on 128-row tiles over the (head, block) segments
-  int64_t max_chunks;      // upper bound on backward chunks
   int idx_tok;             // tokens per index-builder CTA (256, 128, 64 or 32)
   int64_t n_idx_tiles;     // token tiles of the index builder
   int n_w;                 // forward waves (token windows processed one after another)
@@ -40,7 +38,7 @@ struct Layout {
   int64_t max_wtiles;      // upper bound on forward tiles over the sub-segments
   int64_t n_scan_ctas;     // CTAs of the sub-segment tile scan
   // index region
-  size_t status, nb, blk_start, counts, offsets, tile_off, chunk_off, q_list, slot_map,
+  size_t status, nb, blk_start, counts, offsets, tile_off, q_list, slot_map,
       chunk_hist, npairs, cnt, prow, wtile_off, wscan_part, tdesc, tseg;
   size_t index_end;
   // forward scratch
@@ -76,7 +74,7 @@ struct Params {
   void *out, *dq, *dk, *dv;
   float *lse;
   // workspace views
-  int32_t *status, *nb, *blk_start, *counts, *offsets, *tile_off, *chunk_off, *q_list,
+  int32_t *status, *nb, *blk_start, *counts, *offsets, *tile_off, *q_list,
       *slot_map, *chunk_hist, *npairs, *cnt, *prow, *wtile_off, *wscan_part;
   TileDesc *tdesc;
   int32_t *tseg;    // (head, block) segment of every forward tile

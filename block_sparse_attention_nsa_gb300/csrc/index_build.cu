@@ -182,34 +182,32 @@ __global__ void __launch_bounds__(1024) col_scan_kernel(Params p) {
   }
 }
 
-// One block of 1024 threads: offsets (pairs), tile_off (128-row tiles) and
-// chunk_off (backward chunks of up to kBwdChunkTiles tiles) over h_k * nb segments.
+// One block of 1024 threads: offsets (pairs) and tile_off (128-row tiles) over the
+// h_k * nb segments.  With a single forward wave the sub-segments are the segments,
+// and wtile_off (indexed h * nb_max + block) is written here too.
 __global__ void __launch_bounds__(1024) scan_kernel(Params p) {
-  __shared__ int64_t sums[3][32];
+  __shared__ int64_t sums[2][32];
   const int nseg = p.h_k * (*p.nb);
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int per = (nseg + nt - 1) / nt;
   const int i0 = min(nseg, tid * per), i1 = min(nseg, i0 + per);
-  int64_t a = 0, b = 0, c = 0;
+  int64_t a = 0, b = 0;
   for (int i = i0; i < i1; ++i) {
     const int64_t rows = (int64_t)p.counts[i] * p.g;
-    const int64_t tiles = (rows + kTileRows - 1) / kTileRows;
     a += p.counts[i];
-    b += tiles;
-    c += (tiles + kBwdChunkTiles - 1) / kBwdChunkTiles;
+    b += (rows + kTileRows - 1) / kTileRows;
   }
-  int64_t xa = a, xb = b, xc = c;
+  int64_t xa = a, xb = b;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     int64_t ya = __shfl_up_sync(0xffffffffu, xa, o);
     int64_t yb = __shfl_up_sync(0xffffffffu, xb, o);
-    int64_t yc = __shfl_up_sync(0xffffffffu, xc, o);
-    if (lane >= o) { xa += ya; xb += yb; xc += yc; }
+    if (lane >= o) { xa += ya; xb += yb; }
   }
-  if (lane == 31) { sums[0][warp] = xa; sums[1][warp] = xb; sums[2][warp] = xc; }
+  if (lane == 31) { sums[0][warp] = xa; sums[1][warp] = xb; }
   __syncthreads();
   if (warp == 0) {
-    for (int k = 0; k < 3; ++k) {
+    for (int k = 0; k < 2; ++k) {
       int64_t w = lane < (nt >> 5) ? sums[k][lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -222,21 +220,29 @@ __global__ void __launch_bounds__(1024) scan_kernel(Params p) {
   __syncthreads();
   int64_t ra = xa - a + (warp ? sums[0][warp - 1] : 0);
   int64_t rb = xb - b + (warp ? sums[1][warp - 1] : 0);
-  int64_t rc = xc - c + (warp ? sums[2][warp - 1] : 0);
+  const int nb = *p.nb;
   for (int i = i0; i < i1; ++i) {
     p.offsets[i] = static_cast<int32_t>(ra);
     p.tile_off[i] = static_cast<int32_t>(rb);
-    p.chunk_off[i] = static_cast<int32_t>(rc);
+    if (p.n_w == 1) p.wtile_off[(int64_t)(i / nb) * p.nb_max + i % nb] = static_cast<int32_t>(rb);
     const int64_t rows = (int64_t)p.counts[i] * p.g;
-    const int64_t tiles = (rows + kTileRows - 1) / kTileRows;
     ra += p.counts[i];
-    rb += tiles;
-    rc += (tiles + kBwdChunkTiles - 1) / kBwdChunkTiles;
+    rb += (rows + kTileRows - 1) / kTileRows;
   }
   if (tid == nt - 1) {
     p.offsets[nseg] = static_cast<int32_t>(ra);
     p.tile_off[nseg] = static_cast<int32_t>(rb);
-    p.chunk_off[nseg] = static_cast<int32_t>(rc);
+  }
+  if (p.n_w == 1) {
+    // sub-segments of blocks nb .. nb_max - 1 hold no tiles: they start where the
+    // next head's (or, for the last head, the grand total) does
+    __syncthreads();
+    const int64_t pad = p.nb_max - nb;
+    for (int64_t e = tid; e < (int64_t)p.h_k * pad; e += nt) {
+      const int h = static_cast<int>(e / pad), gb = nb + static_cast<int>(e % pad);
+      p.wtile_off[(int64_t)h * p.nb_max + gb] = p.tile_off[(h + 1) * nb];
+    }
+    if (tid == 0) p.wtile_off[p.nsub] = p.tile_off[nseg];
   }
 }
 
@@ -369,12 +375,10 @@ __global__ void __launch_bounds__(256) tile_desc_kernel(Params p) {
 //                                 token t kept block gb;
 //   qbase, pbase [nb_max]:        the block's first q_list position and first
 //                                 forward partial row for this tile's tokens;
-//   wpre [idx_tok / 32][nb_max]:  bytes, tokens of earlier warps that kept gb;
-//   rows [2][idx_tok * T]:        this tile's slot_map and prow rows, written out
-//                                 with coalesced stores.
+//   wpre [idx_tok / 32][nb_max]:  bytes, tokens of earlier warps that kept gb.
 size_t index_scatter_smem(const Params &p) {
   const size_t mw = p.idx_tok / 32;
-  return 4 * (mw * p.nb_max + 2 * p.nb_max + 2 * (size_t)p.idx_tok * p.topk) + mw * p.nb_max + 16;
+  return 4 * (mw * p.nb_max + 2 * p.nb_max) + mw * p.nb_max + 16;
 }
 
 template <int TP>
@@ -385,14 +389,18 @@ __global__ void __launch_bounds__(kIdxThreads) scatter_kernel(Params p) {
   const int mw = p.idx_tok >> 5;
   int32_t *qbase = reinterpret_cast<int32_t *>(masks + mw * p.nb_max);
   int32_t *pbase = qbase + p.nb_max;
-  int32_t *srow = pbase + p.nb_max;                      // [idx_tok * T]
-  int32_t *prow_s = srow + (int64_t)p.idx_tok * p.topk;  // [idx_tok * T]
-  uint8_t *wpre = reinterpret_cast<uint8_t *>(prow_s + (int64_t)p.idx_tok * p.topk);
+  uint8_t *wpre = reinterpret_cast<uint8_t *>(pbase + p.nb_max);
   const int w = tile / p.wave_tiles;
   const int64_t hist_row = ((int64_t)h * p.n_idx_tiles + tile) * p.nb_max;
   const int64_t lo_row = ((int64_t)h * p.n_idx_tiles + (int64_t)w * p.wave_tiles) * p.nb_max;
   const int64_t sub_row = ((int64_t)h * p.n_w + w) * p.nb_max;
-  for (int i = tid; i < mw * nb; i += blockDim.x) masks[i] = 0u;
+  {
+    // mw * nb words from a 16-byte aligned start: four at a time, then the tail
+    uint4 *m4 = reinterpret_cast<uint4 *>(masks);
+    const int nw = mw * nb, n4 = nw >> 2;
+    for (int i = tid; i < n4; i += blockDim.x) m4[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = 4 * n4 + tid; i < nw; i += blockDim.x) masks[i] = 0u;
+  }
   for (int gb = tid; gb < nb; gb += blockDim.x) {
     const int32_t before = p.chunk_hist[hist_row + gb];   // earlier tokens of the block's list
     qbase[gb] = p.offsets[h * nb + gb] + before;
@@ -436,34 +444,43 @@ __global__ void __launch_bounds__(kIdxThreads) scatter_kernel(Params p) {
     }
   }
   __syncthreads();
-  const int ntok = min(p.idx_tok, p.n - t0);
   if (live) {
+    // this token's row of slot_map and prow, computed in registers and written with
+    // 16-byte stores (the rows of a warp's tokens are contiguous)
     const int wl = tid >> 5;
     const uint32_t below = (1u << lane) - 1u;
-    int32_t *srow_t = srow + tid * p.topk;
-    int32_t *prow_t = prow_s + tid * p.topk;
+    int32_t srow[TP], prw[TP];
 #pragma unroll
     for (int k = 0; k < TP; ++k) {
-      if (k >= p.topk) break;
       const int gb = kgb[k];
-      if (gb < 0) {
-        srow_t[k] = -1;
-        prow_t[k] = -1;
-        continue;
+      srow[k] = -1;
+      prw[k] = -1;
+      if (k < p.topk && gb >= 0) {
+        const int32_t r = __popc(masks[wl * nb + gb] & below) + wpre[wl * nb + gb];
+        const int32_t pos = qbase[gb] + r;
+        p.q_list[pos] = t;
+        srow[k] = pos;
+        prw[k] = pbase[gb] + r * p.g;
       }
-      const int32_t r = __popc(masks[wl * nb + gb] & below) + wpre[wl * nb + gb];
-      const int32_t pos = qbase[gb] + r;
-      p.q_list[pos] = t;
-      srow_t[k] = pos;
-      prow_t[k] = pbase[gb] + r * p.g;
     }
-  }
-  __syncthreads();
-  // the tile's rows of slot_map and prow are contiguous: coalesced copies
-  const int64_t base = ((int64_t)h * p.n + t0) * p.topk;
-  for (int i = tid; i < ntok * p.topk; i += blockDim.x) {
-    p.slot_map[base + i] = srow[i];
-    p.prow[base + i] = prow_s[i];
+    const int64_t base = ((int64_t)h * p.n + t) * p.topk;
+    if (TP == p.topk && (TP % 4) == 0) {
+      int4 *ds = reinterpret_cast<int4 *>(p.slot_map + base);
+      int4 *dp = reinterpret_cast<int4 *>(p.prow + base);
+#pragma unroll
+      for (int k = 0; k < TP; k += 4) {
+        ds[k / 4] = make_int4(srow[k], srow[k + 1], srow[k + 2], srow[k + 3]);
+        dp[k / 4] = make_int4(prw[k], prw[k + 1], prw[k + 2], prw[k + 3]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < TP; ++k) {
+        if (k < p.topk) {
+          p.slot_map[base + k] = srow[k];
+          p.prow[base + k] = prw[k];
+        }
+      }
+    }
   }
 }
 
@@ -506,8 +523,10 @@ cudaError_t launch_index(const Params &p, cudaStream_t stream, void (*mark)(int,
   mark(2, stream, false);
   mark(3, stream, true);
   scan_kernel<<<1, 1024, 0, stream>>>(p);
-  wave_scan_local_kernel<<<static_cast<unsigned>(p.n_scan_ctas), 1024, 0, stream>>>(p);
-  wave_scan_add_kernel<<<static_cast<unsigned>(p.n_scan_ctas), 1024, 0, stream>>>(p);
+  if (p.n_w > 1) {   // with one wave scan_kernel has written wtile_off already
+    wave_scan_local_kernel<<<static_cast<unsigned>(p.n_scan_ctas), 1024, 0, stream>>>(p);
+    wave_scan_add_kernel<<<static_cast<unsigned>(p.n_scan_ctas), 1024, 0, stream>>>(p);
+  }
   tile_desc_kernel<<<static_cast<unsigned>((p.nsub + 7) / 8), 256, 0, stream>>>(p);
   mark(3, stream, false);
   mark(4, stream, true);
