@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--extended", action="store_true",
+                    help="also time g = 16, 32K tokens, and (B_K, T) = (128, 8) at d = 64")
     return ap.parse_args()
 
 
@@ -381,9 +383,45 @@ def run_ours(args, rank, world):
                 del rr
                 torch.cuda.empty_cache()
         result["sweep"] = sweep
+    if world == 1 and args.extended:
+        result["extended"] = extended_sweep(torch, dev, pk_burst)
     if rank == 0 and world == 1 and not args.no_cpu and args.cpu_seconds > 0:
         result["cpu_baseline"] = cpu_baseline(cfg, r.host, args.cpu_seconds)
     return result
+
+
+def extended_sweep(torch, dev, pk_burst):
+    """Forward and backward times beyond the headline sweep: g = 16 at 64K tokens,
+    32K-token sequences, and the pages' (B_K, T) = (128, 8) pair (at d = 64: the
+    library does not offer d = 128 with B_K = 128)."""
+    import dataclasses
+    from workloads import CONFIGS
+    base = CONFIGS["fwd64k"]
+    cases = {
+        "64k_g16": base.with_g(16),
+        "32k_g1": dataclasses.replace(base.with_g(1), seqlens=(32768,), name="fwd32k_g1"),
+        "32k_g4": dataclasses.replace(base.with_g(4), seqlens=(32768,), name="fwd32k_g4"),
+        "32k_g16": dataclasses.replace(base.with_g(16), seqlens=(32768,), name="fwd32k_g16"),
+        "64k_d64_b128_t8_g4": dataclasses.replace(base.with_g(4), d=64, block=128, topk=8,
+                                                  name="fwd64k_d64_b128_t8_g4"),
+    }
+    outd = {}
+    for key, c in cases.items():
+        rr = Runner(c, c.seed, dev)
+        ff = useful_fwd_flops(c)
+        rr.step()
+        torch.cuda.synchronize()
+        rr.check_status()
+        f_ms = dist(time_reps(torch, rr.fwd, 20))["median"]
+        b_ms = dist(time_reps(torch, rr.bwd, 20))["median"]
+        outd[key] = {"n": c.n, "g": c.g, "d": c.d, "B_K": c.block, "T": c.topk,
+                     "fwd_ms": f_ms, "bwd_ms": b_ms,
+                     "fwd_tflops": ff / (f_ms * 1e-3) / 1e12,
+                     "bwd_tflops": 2.5 * ff / (b_ms * 1e-3) / 1e12,
+                     "fwd_pct_peak": 100 * ff / (f_ms * 1e-3) / 1e12 / pk_burst}
+        del rr
+        torch.cuda.empty_cache()
+    return outd
 
 
 def run_reference(args, rank, world):

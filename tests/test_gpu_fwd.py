@@ -116,3 +116,21 @@ def test_forward_dense_special_case_matches_sdpa():
     ref_out, ref_lse = oracle.fwd(inp["cu_seqlens"], block, sel, inp["q"], inp["k"], inp["v"],
                                   cfg.scale)
     check_forward(out, lse, ref_out, ref_lse, "dense")
+
+
+@pytest.mark.parametrize("which", ["64k_g16", "64k_d64_b128_t8"])
+def test_forward_extended_sampled(which):
+    # beyond the five workloads: g = 16 at 64K tokens, and the pages' (B_K, T) = (128, 8)
+    # pair at d = 64; sampled rows against the oracle, the whole output finite
+    import dataclasses
+    base = CONFIGS["fwd64k"]
+    cfg = base.with_g(16) if which == "64k_g16" else dataclasses.replace(
+        base.with_g(4), d=64, block=128, topk=8, name="fwd64k_d64_b128_t8")
+    inp = make_inputs(cfg)
+    out, lse = _run(cfg, inp)
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    rows = sample_rows(cfg.n, cfg.h_q, 400, seed=16, block=cfg.block)
+    ref_o, ref_l = oracle.fwd_rows(inp["cu_seqlens"], cfg.block, inp["sel_idx"], inp["q"],
+                                   inp["k"], inp["v"], cfg.scale, rows)
+    check_forward(out[rows[:, 0], rows[:, 1]], lse[rows[:, 1], rows[:, 0]], ref_o, ref_l,
+                  cfg.name)
