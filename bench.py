@@ -421,6 +421,40 @@ def extended_sweep(torch, dev, pk_burst):
                      "fwd_pct_peak": 100 * ff / (f_ms * 1e-3) / 1e12 / pk_burst}
         del rr
         torch.cuda.empty_cache()
+    outd.update(decode_sweep(torch, dev))
+    return outd
+
+
+def decode_sweep(torch, dev):
+    """One-step decode: 64 sequences with 8192-token caches, 4 KV heads, d = 128,
+    B_K = 64, T = 16, distance-weighted selection of the last token.  HBM-bound: the
+    algorithmic bytes are the kept K/V blocks (plus q and out)."""
+    import block_sparse_attention_nsa_gb300 as nsa
+    from workloads import make_decode_inputs
+    outd = {}
+    B, L, h_k, d, blk, T = 64, 8192, 4, 128, 64, 16
+    for g in (4, 16):
+        inp = make_decode_inputs([L] * B, h_k, g, d, blk, T, "distance", "bf16", seed=2000 + g)
+        q, k, v = (inp[x].to(dev) for x in ("q", "k", "v"))
+        sel = torch.from_numpy(inp["sel_idx"]).to(dev)
+        cu = torch.from_numpy(inp["cu_seqlens"]).to(dev)
+        out = torch.empty_like(q)
+        lse = torch.empty((h_k * g, B), dtype=torch.float32, device=dev)
+        run = lambda: nsa.decode(q, k, v, sel, cu, blk, inp["scale"], out=out, lse=lse)
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        ms = dist(time_reps(torch, run, 50))["median"]
+        kept = int((inp["sel_idx"] >= 0).sum())                 # one (head, block) per kept slot
+        kv_bytes = kept * blk * d * 2 * 2
+        io_bytes = 2 * q.numel() * q.element_size() + lse.numel() * 4
+        gbs = (kv_bytes + io_bytes) / (ms * 1e-3) / 1e9
+        outd[f"decode_b{B}_{L // 1024}k_g{g}"] = {
+            "us": ms * 1e3, "algorithmic_bytes": kv_bytes + io_bytes, "GB/s": gbs,
+            "frac_of_measured_hbm": gbs / peaks()[2],
+            "useful_tflops": 4.0 * d * g * kept * blk / (ms * 1e-3) / 1e12}
+        del q, k, v, out
+        torch.cuda.empty_cache()
     return outd
 
 

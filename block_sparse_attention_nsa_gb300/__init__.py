@@ -6,7 +6,7 @@ current stream.  There is no CPU or PyTorch fallback: if the library is missing
 or a call fails, an exception is raised.
 
 Names follow the C ABI in include/nsa_sel_attn.h:
-  workspace_size, index, index_view, fwd, bwd, step_host, get_status,
+  workspace_size, index, index_view, fwd, bwd, decode, step_host, get_status,
   profile_enable, profile_collect.
 """
 from __future__ import annotations
@@ -18,6 +18,7 @@ from typing import Optional
 import torch
 
 __all__ = ["Dims", "NsaError", "load", "workspace_size", "index", "index_view", "fwd", "bwd",
+           "decode",
            "staging_size", "step_host", "get_status", "profile_enable", "profile_collect",
            "kernel_names", "make_dims", "LIB_PATH"]
 
@@ -70,6 +71,7 @@ def load():
         "nsa_sel_attn_step_host": (st, [dp, vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp, vp,
                                         sz, vp, sz, vp]),
         "nsa_sel_attn_get_status": (st, [dp, vp, vp, ctypes.POINTER(i32)]),
+        "nsa_sel_attn_decode": (st, [dp, vp, vp, vp, vp, vp, f32, vp, vp, vp, vp]),
         "nsa_sel_attn_num_kernels": (i32, []),
         "nsa_sel_attn_kernel_name": (ctypes.c_char_p, [i32]),
         "nsa_sel_attn_profile_enable": (st, [i32]),
@@ -219,6 +221,25 @@ def step_host(dims: Dims, host: dict, scale: float, staging: torch.Tensor,
         _ptr(host["out"]), _ptr(host.get("lse")), _ptr(host["dq"]), _ptr(host["dk"]),
         _ptr(host["dv"]), _ptr(staging), staging.numel(), _ptr(workspace), workspace.numel(),
         _stream(stream)), "step_host")
+
+
+def decode(q, k_cache, v_cache, sel_idx, cu_seqlens, block_size: int, scale: float, out=None,
+           lse=None, device_status=None, stream=None):
+    """One-step decode: q [B, h_q, d] (the last token of each cached sequence), caches
+    [N, h_k, d], sel_idx int32 [h_k, B, T]; returns out [B, h_q, d] and lse [h_q, B]."""
+    _contig(q, k_cache, v_cache, sel_idx, cu_seqlens)
+    B, h_q, d = q.shape
+    h_k, topk = k_cache.shape[1], sel_idx.shape[2]
+    dims = make_dims(B, k_cache.shape[0], h_q, h_k, d, block_size, topk, q.dtype)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((h_q, B), dtype=torch.float32, device=q.device)
+    _check(load().nsa_sel_attn_decode(
+        ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(sel_idx),
+        _ptr(cu_seqlens), float(scale), _ptr(out), _ptr(lse), _ptr(device_status),
+        _stream(stream)), "decode")
+    return out, lse
 
 
 def get_status(dims: Dims, workspace: torch.Tensor, stream=None):

@@ -12,6 +12,10 @@ cudaError_t launch_index(const Params &p, cudaStream_t s, void (*mark)(int, cuda
 cudaError_t index_set_smem_limits(const Params &p);
 cudaError_t launch_fwd(const Params &p, int num_sms, int64_t max_tiles, cudaStream_t s,
                        void (*mark)(int, cudaStream_t, bool));
+cudaError_t launch_decode(int num_seqs, int h_q, int h_k, int d, int block, int topk, bool fp16,
+                          float scale, const void *q, const void *k, const void *v,
+                          const int32_t *sel, const int32_t *cu, void *out, float *lse,
+                          int32_t *status, cudaStream_t s);
 cudaError_t launch_bwd(const Params &p, int num_sms, int64_t max_tiles, cudaStream_t s,
                        void (*mark)(int, cudaStream_t, bool));
 
@@ -502,6 +506,26 @@ nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const void *hos
       return NSA_ERR_CUDA;
   if (cudaStreamWaitEvent(s, aux->out_back, 0) != cudaSuccess) return NSA_ERR_CUDA;
   return cuda_status(cudaStreamSynchronize(s));
+}
+
+nsa_status nsa_sel_attn_decode(const nsa_sel_attn_dims *dims, const void *q, const void *k_cache,
+                               const void *v_cache, const int32_t *sel_idx,
+                               const int32_t *cu_seqlens, float scale, void *out, float *lse,
+                               int32_t *device_status, nsa_stream_t stream) {
+  nsa_status st = check_dims(dims, false);
+  if (st != NSA_OK) return st;
+  if (!(dims->head_dim == 64 || dims->head_dim == 128)) return NSA_ERR_UNSUPPORTED;
+  if (dims->h_q / dims->h_k > 16) return NSA_ERR_UNSUPPORTED;
+  if ((int64_t)dims->num_seqs * dims->h_q >= (int64_t(1) << 31)) return NSA_ERR_UNSUPPORTED;
+  if (!cu_seqlens || !q || !sel_idx || !out || !lse) return NSA_ERR_INVALID_ARG;
+  if (dims->total_tokens > 0 && (!k_cache || !v_cache)) return NSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || (device_status && !aligned(device_status, 4)))
+    return NSA_ERR_INVALID_ARG;
+  return cuda_status(launch_decode(dims->num_seqs, dims->h_q, dims->h_k, dims->head_dim,
+                                   dims->block_size, dims->topk, dims->dtype == NSA_FP16, scale,
+                                   q, k_cache, v_cache, sel_idx, cu_seqlens, out, lse,
+                                   device_status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 nsa_status nsa_sel_attn_get_status(const nsa_sel_attn_dims *dims, void *workspace,

@@ -187,6 +187,36 @@ NSA_API nsa_status nsa_sel_attn_fwd_noalloc(const nsa_sel_attn_dims *dims, const
 NSA_API nsa_status nsa_sel_attn_fwd_noalloc_status(const nsa_sel_attn_dims *dims,
                                                    nsa_stream_t stream, int32_t *bits);
 
+/* One-step decode: the one-step decoding preview of the Flash-Sparse-Attention
+ * README ("News"), the decoding stage that the papernotes page leaves open
+ * (局限与展望).  Every sequence b has one new query token, the last token of its KV
+ * cache (local position len_b - 1).  It attends to the keys of the blocks its
+ * selection names, with the forward's arithmetic for that token:
+ *   - the causal mask (every cached key of a kept block, up to the token itself);
+ *   - the same validity, de-duplication and error rules for sel_idx;
+ *   - one softmax over the union of the kept blocks.
+ *   dims:      num_seqs = B sequences; total_tokens = N cached tokens in all;
+ *              h_q, h_k, head_dim, block_size, topk, dtype as for the forward.
+ *              Supported: head_dim 64 or 128, g = h_q / h_k <= 16.
+ *   q:         [B, h_q, d] (dtype), the new token of each sequence.
+ *   k_cache, v_cache: [N, h_k, d] (dtype), packed by cu_seqlens.
+ *   sel_idx:   int32 [h_k, B, T], block indices local to each sequence.
+ *   cu_seqlens: int32 [B + 1], cache offsets (cu[0] = 0, cu[B] = N).
+ *   out:       [B, h_q, d] (dtype); lse: float32 [h_q, B] (natural log, scale
+ *              included; -inf and out = 0 for a sequence with no kept key).
+ *   device_status: optional int32 in device memory.  NSA_DEVERR_BAD_INDEX is ORed
+ *              into it for a value < -1 or past the sequence's last block; NULL
+ *              skips the report.
+ * No workspace: one CTA per (sequence, KV head) merges its warps' partial results on
+ * chip.  Asynchronous on `stream`; q, caches and out 16-byte aligned.  The pages give
+ * no decode algorithm; this entry point is the forward restricted to one token per
+ * sequence. */
+NSA_API nsa_status nsa_sel_attn_decode(const nsa_sel_attn_dims *dims, const void *q,
+                                       const void *k_cache, const void *v_cache,
+                                       const int32_t *sel_idx, const int32_t *cu_seqlens,
+                                       float scale, void *out, float *lse,
+                                       int32_t *device_status, nsa_stream_t stream);
+
 /* Synchronises `stream`, reads and clears the device status word of this
  * workspace.  Returns NSA_OK, NSA_ERR_BAD_INDEX or NSA_ERR_TIMEOUT (the worst
  * seen) and stores the raw bits in *bits when bits is not NULL. */

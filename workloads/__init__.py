@@ -132,6 +132,44 @@ def make_selection(seqlens: Sequence[int], h_k: int, block: int, topk: int, rule
     return np.ascontiguousarray(np.concatenate(parts, axis=1))
 
 
+def _draw_last_token(rng: np.random.Generator, length: int, h_k: int, block: int, topk: int,
+                     rule: str) -> np.ndarray:
+    """Selection row [h_k, topk] of the last token of a sequence of `length` tokens, by
+    the same rule as _draw_one_sequence (own block, block 0, draws from 1 .. c-1)."""
+    sel = np.full((h_k, topk), -1, dtype=np.int32)
+    if length <= 0:
+        return sel
+    c = (length - 1) // block
+    sel[:, 0] = c
+    if topk >= 2 and c > 0:
+        sel[:, 1] = 0
+    ndraw = min(topk - 2, c - 1) if topk >= 2 else 0
+    if ndraw > 0:
+        cand = np.arange(1, c, dtype=np.int32)
+        logw = (np.zeros(c - 1) if rule == "uniform"
+                else -np.log1p((c - cand).astype(np.float64)))
+        keys = logw[None, :] + rng.gumbel(size=(h_k, c - 1))
+        picks = np.argsort(-keys, axis=-1, kind="stable")[:, :ndraw]
+        sel[:, 2:2 + ndraw] = cand[picks]
+    return sel
+
+
+def make_decode_inputs(seqlens: Sequence[int], h_k: int, g: int, d: int, block: int, topk: int,
+                       rule: str, dtype: str, seed: int, std: float = 1.0):
+    """One-step decode inputs: q [B, h_q, d] (the new token of each sequence), k/v caches
+    [N, h_k, d] packed by cu_seqlens, sel_idx int32 [h_k, B, T] (the last token's row)."""
+    rng = np.random.default_rng(seed)
+    td = torch_dtype(dtype)
+    B, n = len(seqlens), int(np.sum(seqlens))
+    q = _normal(rng, (B, h_k * g, d), std, td)
+    k = _normal(rng, (n, h_k, d), std, td)
+    v = _normal(rng, (n, h_k, d), std, td)
+    sel = np.stack([_draw_last_token(rng, int(L), h_k, block, topk, rule) for L in seqlens],
+                   axis=1)
+    return {"q": q, "k": k, "v": v, "sel_idx": np.ascontiguousarray(sel),
+            "cu_seqlens": make_cu_seqlens(seqlens), "scale": d ** -0.5}
+
+
 def _normal(rng: np.random.Generator, shape, std: float, dtype: torch.dtype) -> torch.Tensor:
     x = rng.standard_normal(size=shape, dtype=np.float32)
     if std != 1.0:
