@@ -17,6 +17,11 @@ Parity status per function (pins live in tests/test_oracle_*.py):
   index          -- pinned: brute-force construction on tiny inputs, the
                     scan/segment/inverse invariants, and the closed-form pair
                     counts of the synthetic selection rule.
+  window_select, fwd / bwd with window -- pinned: dense sliding-window attention
+                    (torch SDPA with a band mask, fp64) and its autograd; window
+                    >= sequence length equals plain causal attention.
+  gate_combine / gate_combine_bwd -- pinned: closed-form sums and central finite
+                    differences of the gates.
 """
 from __future__ import annotations
 
@@ -74,6 +79,15 @@ def _load():
         lib.nsa_oracle_index.restype = c_i64
         lib.nsa_oracle_num_blocks.argtypes = [c_int, _i32p, c_int]
         lib.nsa_oracle_num_blocks.restype = c_i64
+        lib.nsa_oracle_fwd_w.argtypes = [c_int, _i32p, c_int, c_int, c_int, c_int, c_int, c_int,
+                                         _i32p, _f64p, _f64p, _f64p, c_dbl, _f64p, _f64p, c_int]
+        lib.nsa_oracle_fwd_w.restype = c_int
+        lib.nsa_oracle_bwd_w.argtypes = [c_int, _i32p, c_int, c_int, c_int, c_int, c_int, c_int,
+                                         _i32p, _f64p, _f64p, _f64p, _f64p, c_dbl, _f64p, _f64p,
+                                         _f64p, c_int]
+        lib.nsa_oracle_bwd_w.restype = c_int
+        lib.nsa_oracle_window_select.argtypes = [c_int, _i32p, c_int, c_int, c_int, c_int, _i32p]
+        lib.nsa_oracle_window_select.restype = c_int
         lib.nsa_oracle_max_threads.argtypes = []
         lib.nsa_oracle_max_threads.restype = c_int
         _lib = lib
@@ -109,15 +123,16 @@ def _dims(cu, q, k, sel):
     return n, h_q, h_k, h_q // h_k, d, topk
 
 
-def fwd(cu_seqlens, block, sel_idx, q, k, v, scale, threads: int = 0):
-    """out [N, h_q, d] and lse [h_q, N] in fp64 (natural log, scale included)."""
+def fwd(cu_seqlens, block, sel_idx, q, k, v, scale, threads: int = 0, window: int = 0):
+    """out [N, h_q, d] and lse [h_q, N] in fp64 (natural log, scale included).  window
+    > 0 also restricts every token's keys to its last `window` positions."""
     cu, sel = _i32(cu_seqlens), _i32(sel_idx)
     q, k, v = _f64(q), _f64(k), _f64(v)
     n, h_q, h_k, g, d, topk = _dims(cu, q, k, sel)
     out = np.empty((n, h_q, d))
     lse = np.empty((h_q, n))
-    rc = _load().nsa_oracle_fwd(len(cu) - 1, cu, h_k, g, d, block, topk, sel, q, k, v,
-                                float(scale), out, lse, threads)
+    rc = _load().nsa_oracle_fwd_w(len(cu) - 1, cu, h_k, g, d, block, topk, int(window), sel, q,
+                                  k, v, float(scale), out, lse, threads)
     if rc:
         raise RuntimeError(f"nsa_oracle_fwd failed ({rc})")
     return out, lse
@@ -138,19 +153,49 @@ def fwd_rows(cu_seqlens, block, sel_idx, q, k, v, scale, rows, threads: int = 0)
     return out, lse
 
 
-def bwd(cu_seqlens, block, sel_idx, q, k, v, dout, scale, threads: int = 0):
-    """dq [N, h_q, d], dk, dv [N, h_k, d] in fp64 by direct differentiation."""
+def bwd(cu_seqlens, block, sel_idx, q, k, v, dout, scale, threads: int = 0, window: int = 0):
+    """dq [N, h_q, d], dk, dv [N, h_k, d] in fp64 by direct differentiation (window as
+    for fwd)."""
     cu, sel = _i32(cu_seqlens), _i32(sel_idx)
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     n, h_q, h_k, g, d, topk = _dims(cu, q, k, sel)
     dq = np.empty((n, h_q, d))
     dk = np.empty((n, h_k, d))
     dv = np.empty((n, h_k, d))
-    rc = _load().nsa_oracle_bwd(len(cu) - 1, cu, h_k, g, d, block, topk, sel, q, k, v, dout,
-                                float(scale), dq, dk, dv, threads)
+    rc = _load().nsa_oracle_bwd_w(len(cu) - 1, cu, h_k, g, d, block, topk, int(window), sel, q,
+                                  k, v, dout, float(scale), dq, dk, dv, threads)
     if rc:
         raise RuntimeError(f"nsa_oracle_bwd failed ({rc})")
     return dq, dk, dv
+
+
+def window_select(cu_seqlens, h_k, block, topk, window) -> np.ndarray:
+    """Selection int32 [h_k, N, topk] of the sliding window: the blocks holding the keys
+    of (tau - window, tau] of each token, newest first, the rest -1."""
+    cu = _i32(cu_seqlens)
+    n = int(cu[-1])
+    sel = np.empty((h_k, n, topk), dtype=np.int32)
+    if _load().nsa_oracle_window_select(len(cu) - 1, cu, h_k, block, topk, int(window), sel):
+        raise ValueError("topk too small for the window")
+    return sel
+
+
+def gate_combine(branches, gates):
+    """Gated combination of branch outputs (the three-branch NSA output): out[r] =
+    sum_b gates[r, b] * o_b[r].  branches: list of [N, h_q, d]; gates [N, h_q, nb]."""
+    g = _f64(gates)
+    out = np.zeros(_f64(branches[0]).shape)
+    for b, o in enumerate(branches):
+        out += g[..., b:b + 1] * _f64(o)
+    return out
+
+
+def gate_combine_bwd(branches, gates, dout):
+    """d o_b = gates[..., b] * dout; d gates[..., b] = sum_d dout * o_b."""
+    g, dy = _f64(gates), _f64(dout)
+    d_br = [g[..., b:b + 1] * dy for b in range(len(branches))]
+    d_g = np.stack([(dy * _f64(o)).sum(-1) for o in branches], axis=-1)
+    return d_br, d_g
 
 
 def num_blocks(cu_seqlens, block) -> int:

@@ -105,8 +105,11 @@ static int token_blocks(const int32_t *row, int topk, int c, int nblk, int *bloc
     return n;
 }
 
-/* Local key indices K(t) (ascending); returns |K(t)|. */
-static int token_keys(const int32_t *row, int topk, int tau, int len, int block, int *keys) {
+/* Local key indices K(t) (ascending); returns |K(t)|.  With window > 0 (the
+ * sliding-window branch, window_size of the Flash-Sparse-Attention README) a key is
+ * also required to lie in the window: kappa > tau - window. */
+static int token_keys(const int32_t *row, int topk, int tau, int len, int block, int window,
+                      int *keys) {
     int blocks[ORC_MAX_TOPK];
     int c = tau / block, nblk = (len + block - 1) / block;
     int nb = token_blocks(row, topk, c, nblk, blocks), n = 0;
@@ -114,6 +117,7 @@ static int token_keys(const int32_t *row, int topk, int tau, int len, int block,
         for (int j = 0; j < block; ++j) {
             int kappa = blocks[i] * block + j;
             if (kappa > tau) break;
+            if (window > 0 && kappa <= tau - window) continue;
             keys[n++] = kappa;
         }
     return n;
@@ -137,13 +141,15 @@ static int check_args(int num_seqs, const int32_t *cu, int h_k, int g, int d, in
 /* Forward for one (token, query head): writes o[d] and returns lse.  Scratch: keys
  * and scores of size topk*block. */
 static double fwd_one(const int32_t *cu, int num_seqs, int h_k, int g, int d, int block, int topk,
-                      const int32_t *sel, const double *q, const double *k, const double *v,
-                      double scale, int64_t t, int hq, double *o, int *keys, double *sc) {
+                      int window, const int32_t *sel, const double *q, const double *k,
+                      const double *v, double scale, int64_t t, int hq, double *o, int *keys,
+                      double *sc) {
     const int64_t N = cu[num_seqs];
     const int h_q = h_k * g, h = hq / g;
     const int s = seq_of(cu, num_seqs, t);
     const int tau = (int)(t - cu[s]), len = cu[s + 1] - cu[s];
-    const int nk = token_keys(sel + ((int64_t)h * N + t) * topk, topk, tau, len, block, keys);
+    const int nk =
+        token_keys(sel + ((int64_t)h * N + t) * topk, topk, tau, len, block, window, keys);
     const double *qt = q + (t * h_q + hq) * d;
     for (int i = 0; i < d; ++i) o[i] = 0.0;
     if (nk == 0) return -INFINITY;
@@ -164,9 +170,9 @@ static double fwd_one(const int32_t *cu, int num_seqs, int h_k, int g, int d, in
     return lse;
 }
 
-int nsa_oracle_fwd(int num_seqs, const int32_t *cu, int h_k, int g, int d, int block, int topk,
-                   const int32_t *sel, const double *q, const double *k, const double *v,
-                   double scale, double *out, double *lse, int num_threads) {
+int nsa_oracle_fwd_w(int num_seqs, const int32_t *cu, int h_k, int g, int d, int block, int topk,
+                     int window, const int32_t *sel, const double *q, const double *k,
+                     const double *v, double scale, double *out, double *lse, int num_threads) {
     if (check_args(num_seqs, cu, h_k, g, d, block, topk)) return 1;
     set_threads(num_threads);
     const int64_t N = cu[num_seqs];
@@ -182,13 +188,21 @@ int nsa_oracle_fwd(int num_seqs, const int32_t *cu, int h_k, int g, int d, int b
             if (!keys || !sc) continue;
             int64_t t = i / h_q;
             int hq = (int)(i % h_q);
-            lse[(int64_t)hq * N + t] = fwd_one(cu, num_seqs, h_k, g, d, block, topk, sel, q, k, v,
-                                               scale, t, hq, out + (t * h_q + hq) * d, keys, sc);
+            lse[(int64_t)hq * N + t] = fwd_one(cu, num_seqs, h_k, g, d, block, topk, window, sel,
+                                               q, k, v, scale, t, hq, out + (t * h_q + hq) * d,
+                                               keys, sc);
         }
         free(keys);
         free(sc);
     }
     return bad ? 2 : 0;
+}
+
+int nsa_oracle_fwd(int num_seqs, const int32_t *cu, int h_k, int g, int d, int block, int topk,
+                   const int32_t *sel, const double *q, const double *k, const double *v,
+                   double scale, double *out, double *lse, int num_threads) {
+    return nsa_oracle_fwd_w(num_seqs, cu, h_k, g, d, block, topk, 0, sel, q, k, v, scale, out,
+                            lse, num_threads);
 }
 
 /* Forward on selected (token, query head) pairs only: rows[2*i] = t, rows[2*i+1] = hq;
@@ -212,7 +226,7 @@ int nsa_oracle_fwd_rows(int num_seqs, const int32_t *cu, int h_k, int g, int d, 
 #pragma omp for schedule(dynamic, 16)
         for (int64_t i = 0; i < n_rows; ++i) {
             if (!keys || !sc) continue;
-            lse_rows[i] = fwd_one(cu, num_seqs, h_k, g, d, block, topk, sel, q, k, v, scale,
+            lse_rows[i] = fwd_one(cu, num_seqs, h_k, g, d, block, topk, 0, sel, q, k, v, scale,
                                   rows[2 * i], (int)rows[2 * i + 1], out_rows + i * d, keys, sc);
         }
         free(keys);
@@ -228,10 +242,10 @@ int nsa_oracle_fwd_rows(int num_seqs, const int32_t *cu, int h_k, int g, int d, 
  * set K(t) contains key j.  No blocking beyond the definition; the pass split only
  * keeps the parallel loops free of write conflicts.
  */
-int nsa_oracle_bwd(int num_seqs, const int32_t *cu, int h_k, int g, int d, int block, int topk,
-                   const int32_t *sel, const double *q, const double *k, const double *v,
-                   const double *dout, double scale, double *dq, double *dk, double *dv,
-                   int num_threads) {
+int nsa_oracle_bwd_w(int num_seqs, const int32_t *cu, int h_k, int g, int d, int block, int topk,
+                     int window, const int32_t *sel, const double *q, const double *k,
+                     const double *v, const double *dout, double scale, double *dq, double *dk,
+                     double *dv, int num_threads) {
     if (check_args(num_seqs, cu, h_k, g, d, block, topk)) return 1;
     set_threads(num_threads);
     const int64_t N = cu[num_seqs];
@@ -256,7 +270,8 @@ int nsa_oracle_bwd(int num_seqs, const int32_t *cu, int h_k, int g, int d, int b
             const int tau = (int)(t - cu[s]), len = cu[s + 1] - cu[s];
             double *dqt = dq + (t * h_q + hq) * d;
             for (int x = 0; x < d; ++x) dqt[x] = 0.0;
-            const int nk = token_keys(sel + ((int64_t)h * N + t) * topk, topk, tau, len, block, keys);
+            const int nk = token_keys(sel + ((int64_t)h * N + t) * topk, topk, tau, len, block,
+                                      window, keys);
             if (nk == 0) { lse[i] = -INFINITY; Dt[i] = 0.0; continue; }
             const double *qt = q + (t * h_q + hq) * d;
             const double *dot_ = dout + (t * h_q + hq) * d;
@@ -318,6 +333,7 @@ int nsa_oracle_bwd(int num_seqs, const int32_t *cu, int h_k, int g, int d, int b
                 for (int i = 0; i < block; ++i) {
                     const int kappa = b * block + i;
                     if (kappa > tau) break;
+                    if (window > 0 && kappa <= tau - window) continue;
                     const int64_t kt = cu[s] + kappa;
                     const double *kj = k + (kt * h_k + h) * d, *vj = v + (kt * h_k + h) * d;
                     const double p = exp(scale * dot(qt, kj, d) - L);
@@ -333,6 +349,34 @@ int nsa_oracle_bwd(int num_seqs, const int32_t *cu, int h_k, int g, int d, int b
     }
     free(lse);
     free(Dt);
+    return 0;
+}
+
+int nsa_oracle_bwd(int num_seqs, const int32_t *cu, int h_k, int g, int d, int block, int topk,
+                   const int32_t *sel, const double *q, const double *k, const double *v,
+                   const double *dout, double scale, double *dq, double *dk, double *dv,
+                   int num_threads) {
+    return nsa_oracle_bwd_w(num_seqs, cu, h_k, g, d, block, topk, 0, sel, q, k, v, dout, scale,
+                            dq, dk, dv, num_threads);
+}
+
+/* Selection rows of the sliding window: token t (local position tau) names the blocks
+ * that hold keys of (tau - window, tau], newest first (c, c - 1, ...), the rest -1.
+ * Returns 1 when topk is too small for some token. */
+int nsa_oracle_window_select(int num_seqs, const int32_t *cu, int h_k, int block, int topk,
+                             int window, int32_t *sel) {
+    const int64_t N = cu[num_seqs];
+    for (int s = 0; s < num_seqs; ++s)
+        for (int tau = 0; tau < cu[s + 1] - cu[s]; ++tau) {
+            const int64_t t = cu[s] + tau;
+            const int c = tau / block;
+            const int first = tau - window + 1 > 0 ? (tau - window + 1) / block : 0;
+            if (c - first + 1 > topk) return 1;
+            for (int h = 0; h < h_k; ++h) {
+                int32_t *row = sel + ((int64_t)h * N + t) * topk;
+                for (int k = 0; k < topk; ++k) row[k] = (c - k >= first) ? c - k : -1;
+            }
+        }
     return 0;
 }
 
