@@ -18,7 +18,8 @@ from typing import Optional
 import torch
 
 __all__ = ["Dims", "NsaError", "load", "workspace_size", "index", "index_view", "fwd", "bwd",
-           "decode",
+           "decode", "window_select", "fwd_window", "bwd_window", "gate_combine",
+           "gate_combine_bwd",
            "staging_size", "step_host", "get_status", "profile_enable", "profile_collect",
            "kernel_names", "make_dims", "LIB_PATH"]
 
@@ -72,6 +73,14 @@ def load():
                                         sz, vp, sz, vp]),
         "nsa_sel_attn_get_status": (st, [dp, vp, vp, ctypes.POINTER(i32)]),
         "nsa_sel_attn_decode": (st, [dp, vp, vp, vp, vp, vp, f32, vp, vp, vp, vp]),
+        "nsa_sel_attn_window_select": (st, [dp, vp, ctypes.c_int, vp, vp]),
+        "nsa_sel_attn_fwd_window": (st, [dp, vp, vp, vp, vp, vp, f32, ctypes.c_int, vp, vp, vp,
+                                         sz, vp]),
+        "nsa_sel_attn_bwd_window": (st, [dp, vp, vp, vp, vp, vp, f32, ctypes.c_int, vp, vp, vp,
+                                         vp, vp, vp, vp, sz, ctypes.c_int, vp]),
+        "nsa_gate_combine_fwd": (st, [dp, ctypes.c_int, vp, vp, vp, vp, vp, vp]),
+        "nsa_gate_combine_bwd": (st, [dp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      vp]),
         "nsa_sel_attn_num_kernels": (i32, []),
         "nsa_sel_attn_kernel_name": (ctypes.c_char_p, [i32]),
         "nsa_sel_attn_profile_enable": (st, [i32]),
@@ -240,6 +249,80 @@ def decode(q, k_cache, v_cache, sel_idx, cu_seqlens, block_size: int, scale: flo
         _ptr(cu_seqlens), float(scale), _ptr(out), _ptr(lse), _ptr(device_status),
         _stream(stream)), "decode")
     return out, lse
+
+
+def window_select(cu_seqlens, total_tokens: int, h_k: int, block_size: int, topk: int,
+                  window: int, num_seqs: Optional[int] = None, stream=None):
+    """Selection int32 [h_k, N, topk] of the sliding window (newest block first)."""
+    num_seqs = cu_seqlens.numel() - 1 if num_seqs is None else num_seqs
+    dims = make_dims(num_seqs, total_tokens, h_k, h_k, 64, block_size, topk, torch.bfloat16)
+    sel = torch.empty((h_k, total_tokens, topk), dtype=torch.int32, device=cu_seqlens.device)
+    _check(load().nsa_sel_attn_window_select(ctypes.byref(dims), _ptr(cu_seqlens), int(window),
+                                             _ptr(sel), _stream(stream)), "window_select")
+    return sel
+
+
+def fwd_window(q, k, v, sel_idx, cu_seqlens, block_size: int, scale: float, window: int,
+               workspace: Optional[torch.Tensor] = None, out=None, lse=None, stream=None):
+    """fwd with the sliding window's lower key bound (keys > t - window)."""
+    _contig(q, k, v, sel_idx, cu_seqlens)
+    dims = _dims_of(q, k, sel_idx, cu_seqlens, block_size)
+    if workspace is None:
+        workspace = alloc_workspace(dims, q.device)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device) \
+        if lse is None else lse
+    _check(load().nsa_sel_attn_fwd_window(
+        ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(sel_idx), _ptr(cu_seqlens),
+        float(scale), int(window), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _stream(stream)), "fwd_window")
+    return out, lse
+
+
+def bwd_window(q, k, v, sel_idx, cu_seqlens, block_size: int, scale: float, window: int, out,
+               lse, dout, workspace: Optional[torch.Tensor] = None, index_ready: bool = False,
+               stream=None):
+    """bwd with the sliding window's lower key bound; returns dq, dk, dv."""
+    _contig(q, k, v, sel_idx, cu_seqlens, out, lse, dout)
+    dims = _dims_of(q, k, sel_idx, cu_seqlens, block_size)
+    if workspace is None:
+        workspace = alloc_workspace(dims, q.device)
+        index_ready = False
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    _check(load().nsa_sel_attn_bwd_window(
+        ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(sel_idx), _ptr(cu_seqlens),
+        float(scale), int(window), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+        _ptr(dv), _ptr(workspace), workspace.numel(), 1 if index_ready else 0, _stream(stream)),
+        "bwd_window")
+    return dq, dk, dv
+
+
+def gate_combine(branches, gates, stream=None):
+    """out = sum_b gates[..., b] * branches[b]; branches [N, h_q, d], gates fp32 [N, h_q, nb]."""
+    _contig(*branches, gates)
+    o = list(branches) + [None] * (3 - len(branches))
+    N, h_q, d = branches[0].shape
+    dims = make_dims(1, N, h_q, h_q, d, 64, 1, branches[0].dtype)
+    out = torch.empty_like(branches[0])
+    _check(load().nsa_gate_combine_fwd(ctypes.byref(dims), len(branches), _ptr(o[0]), _ptr(o[1]),
+                                       _ptr(o[2]), _ptr(gates), _ptr(out), _stream(stream)),
+           "gate_combine")
+    return out
+
+
+def gate_combine_bwd(branches, gates, dout, stream=None):
+    """(list of d branch, d gates fp32)."""
+    _contig(*branches, gates, dout)
+    o = list(branches) + [None] * (3 - len(branches))
+    N, h_q, d = branches[0].shape
+    dims = make_dims(1, N, h_q, h_q, d, 64, 1, branches[0].dtype)
+    dbr = [torch.empty_like(b) for b in branches] + [None] * (3 - len(branches))
+    dg = torch.empty_like(gates)
+    _check(load().nsa_gate_combine_bwd(ctypes.byref(dims), len(branches), _ptr(o[0]), _ptr(o[1]),
+                                       _ptr(o[2]), _ptr(gates), _ptr(dout), _ptr(dbr[0]),
+                                       _ptr(dbr[1]), _ptr(dbr[2]), _ptr(dg), _stream(stream)),
+           "gate_combine_bwd")
+    return dbr[:len(branches)], dg
 
 
 def get_status(dims: Dims, workspace: torch.Tensor, stream=None):

@@ -12,6 +12,12 @@ cudaError_t launch_index(const Params &p, cudaStream_t s, void (*mark)(int, cuda
 cudaError_t index_set_smem_limits(const Params &p);
 cudaError_t launch_fwd(const Params &p, int num_sms, int64_t max_tiles, cudaStream_t s,
                        void (*mark)(int, cudaStream_t, bool));
+cudaError_t launch_window_select(const int32_t *cu, int num_seqs, int n, int h_k, int block,
+                                 int topk, int window, int32_t *sel, cudaStream_t s);
+cudaError_t launch_gate_combine(int64_t rows, int d, bool fp16, int nbr, const void *o0,
+                                const void *o1, const void *o2, const float *gates, void *out,
+                                const void *dout, void *d0, void *d1, void *d2, float *dgates,
+                                bool bwd, cudaStream_t s);
 cudaError_t launch_decode(int num_seqs, int h_q, int h_k, int d, int block, int topk, bool fp16,
                           float scale, const void *q, const void *k, const void *v,
                           const int32_t *sel, const int32_t *cu, void *out, float *lse,
@@ -170,7 +176,6 @@ nsa_status make_layout(const nsa_sel_attn_dims *d, Layout *L) {
   L->slot_map = take(4 * hnt);
   L->chunk_hist = take(4 * static_cast<size_t>(h_k * L->n_idx_tiles * L->nb_max));
   L->npairs = take(4 * hn);
-  L->cnt = take(4 * hn);
   L->prow = take(4 * hnt);
   L->wtile_off = take(4 * static_cast<size_t>(L->nsub + 1));
   L->wscan_part = take(4 * static_cast<size_t>(L->n_scan_ctas));
@@ -215,7 +220,6 @@ void fill_params(Params *p, const nsa_sel_attn_dims *d, const Layout &L, void *w
   p->slot_map = reinterpret_cast<int32_t *>(w + L.slot_map);
   p->chunk_hist = reinterpret_cast<int32_t *>(w + L.chunk_hist);
   p->npairs = reinterpret_cast<int32_t *>(w + L.npairs);
-  p->cnt = reinterpret_cast<int32_t *>(w + L.cnt);
   p->prow = reinterpret_cast<int32_t *>(w + L.prow);
   p->wtile_off = reinterpret_cast<int32_t *>(w + L.wtile_off);
   p->wscan_part = reinterpret_cast<int32_t *>(w + L.wscan_part);
@@ -306,10 +310,10 @@ nsa_status nsa_sel_attn_index_view(const nsa_sel_attn_dims *dims, const void *wo
   return NSA_OK;
 }
 
-nsa_status nsa_sel_attn_fwd(const nsa_sel_attn_dims *dims, const void *q, const void *k,
-                            const void *v, const int32_t *sel_idx, const int32_t *cu_seqlens,
-                            float scale, void *out, float *lse, void *workspace,
-                            size_t workspace_bytes, nsa_stream_t stream) {
+static nsa_status fwd_impl(const nsa_sel_attn_dims *dims, const void *q, const void *k,
+                           const void *v, const int32_t *sel_idx, const int32_t *cu_seqlens,
+                           float scale, int window, void *out, float *lse, void *workspace,
+                           size_t workspace_bytes, nsa_stream_t stream) {
   nsa_status st = check_dims(dims, false);
   if (st != NSA_OK) return st;
   st = check_kernels(dims);
@@ -337,16 +341,35 @@ nsa_status nsa_sel_attn_fwd(const nsa_sel_attn_dims *dims, const void *q, const 
   p.lse = lse;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.window = window;
   st = run_index(dims, L, p, s);
   if (st != NSA_OK) return st;
   return cuda_status(launch_fwd(p, num_sms_cached(), L.max_wtiles, s, mark));
 }
 
-nsa_status nsa_sel_attn_bwd(const nsa_sel_attn_dims *dims, const void *q, const void *k,
+nsa_status nsa_sel_attn_fwd(const nsa_sel_attn_dims *dims, const void *q, const void *k,
                             const void *v, const int32_t *sel_idx, const int32_t *cu_seqlens,
-                            float scale, const void *out, const float *lse, const void *dout,
-                            void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
-                            int index_ready, nsa_stream_t stream) {
+                            float scale, void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, nsa_stream_t stream) {
+  return fwd_impl(dims, q, k, v, sel_idx, cu_seqlens, scale, 0, out, lse, workspace,
+                  workspace_bytes, stream);
+}
+
+nsa_status nsa_sel_attn_fwd_window(const nsa_sel_attn_dims *dims, const void *q, const void *k,
+                                   const void *v, const int32_t *sel_idx,
+                                   const int32_t *cu_seqlens, float scale, int window, void *out,
+                                   float *lse, void *workspace, size_t workspace_bytes,
+                                   nsa_stream_t stream) {
+  if (window < 1) return NSA_ERR_INVALID_ARG;
+  return fwd_impl(dims, q, k, v, sel_idx, cu_seqlens, scale, window, out, lse, workspace,
+                  workspace_bytes, stream);
+}
+
+static nsa_status bwd_impl(const nsa_sel_attn_dims *dims, const void *q, const void *k,
+                           const void *v, const int32_t *sel_idx, const int32_t *cu_seqlens,
+                           float scale, int window, const void *out, const float *lse,
+                           const void *dout, void *dq, void *dk, void *dv, void *workspace,
+                           size_t workspace_bytes, int index_ready, nsa_stream_t stream) {
   nsa_status st = check_dims(dims, true);
   if (st != NSA_OK) return st;
   st = check_kernels(dims);
@@ -380,11 +403,82 @@ nsa_status nsa_sel_attn_bwd(const nsa_sel_attn_dims *dims, const void *q, const 
   p.dv = dv;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.window = window;
   if (!index_ready) {
     st = run_index(dims, L, p, s);
     if (st != NSA_OK) return st;
   }
   return cuda_status(launch_bwd(p, num_sms_cached(), L.max_wtiles, s, mark));
+}
+
+nsa_status nsa_sel_attn_bwd(const nsa_sel_attn_dims *dims, const void *q, const void *k,
+                            const void *v, const int32_t *sel_idx, const int32_t *cu_seqlens,
+                            float scale, const void *out, const float *lse, const void *dout,
+                            void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                            int index_ready, nsa_stream_t stream) {
+  return bwd_impl(dims, q, k, v, sel_idx, cu_seqlens, scale, 0, out, lse, dout, dq, dk, dv,
+                  workspace, workspace_bytes, index_ready, stream);
+}
+
+nsa_status nsa_sel_attn_bwd_window(const nsa_sel_attn_dims *dims, const void *q, const void *k,
+                                   const void *v, const int32_t *sel_idx,
+                                   const int32_t *cu_seqlens, float scale, int window,
+                                   const void *out, const float *lse, const void *dout, void *dq,
+                                   void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                                   int index_ready, nsa_stream_t stream) {
+  if (window < 1) return NSA_ERR_INVALID_ARG;
+  return bwd_impl(dims, q, k, v, sel_idx, cu_seqlens, scale, window, out, lse, dout, dq, dk, dv,
+                  workspace, workspace_bytes, index_ready, stream);
+}
+
+nsa_status nsa_sel_attn_window_select(const nsa_sel_attn_dims *dims, const int32_t *cu_seqlens,
+                                      int window, int32_t *sel_idx, nsa_stream_t stream) {
+  nsa_status st = check_dims(dims, false);
+  if (st != NSA_OK) return st;
+  if (!cu_seqlens || window < 1 || (dims->total_tokens > 0 && !sel_idx))
+    return NSA_ERR_INVALID_ARG;
+  // blocks that can hold keys of a window: ceil((window - 1) / B_K) + 1
+  if (dims->topk < (window - 1 + dims->block_size - 1) / dims->block_size + 1)
+    return NSA_ERR_INVALID_ARG;
+  return cuda_status(launch_window_select(cu_seqlens, dims->num_seqs, dims->total_tokens,
+                                          dims->h_k, dims->block_size, dims->topk, window,
+                                          sel_idx, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nsa_status nsa_gate_combine_fwd(const nsa_sel_attn_dims *dims, int n_branch, const void *o0,
+                                const void *o1, const void *o2, const float *gates, void *out,
+                                nsa_stream_t stream) {
+  nsa_status st = check_dims(dims, false);
+  if (st != NSA_OK) return st;
+  if (n_branch < 1 || n_branch > 3 || !gates || !out || !o0 || (n_branch > 1 && !o1) ||
+      (n_branch > 2 && !o2))
+    return NSA_ERR_INVALID_ARG;
+  if (!aligned(o0, 4) || !aligned(o1, 4) || !aligned(o2, 4) || !aligned(out, 4) ||
+      !aligned(gates, 4))
+    return NSA_ERR_INVALID_ARG;
+  return cuda_status(launch_gate_combine((int64_t)dims->total_tokens * dims->h_q, dims->head_dim,
+                                         dims->dtype == NSA_FP16, n_branch, o0, o1, o2, gates,
+                                         out, nullptr, nullptr, nullptr, nullptr, nullptr, false,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nsa_status nsa_gate_combine_bwd(const nsa_sel_attn_dims *dims, int n_branch, const void *o0,
+                                const void *o1, const void *o2, const float *gates,
+                                const void *dout, void *do0, void *do1, void *do2,
+                                float *dgates, nsa_stream_t stream) {
+  nsa_status st = check_dims(dims, false);
+  if (st != NSA_OK) return st;
+  if (n_branch < 1 || n_branch > 3 || !gates || !dout || !dgates || !o0 ||
+      (n_branch > 1 && !o1) || (n_branch > 2 && !o2))
+    return NSA_ERR_INVALID_ARG;
+  if (!aligned(o0, 4) || !aligned(o1, 4) || !aligned(o2, 4) || !aligned(dout, 4) ||
+      !aligned(do0, 4) || !aligned(do1, 4) || !aligned(do2, 4) || !aligned(gates, 4) ||
+      !aligned(dgates, 4))
+    return NSA_ERR_INVALID_ARG;
+  return cuda_status(launch_gate_combine((int64_t)dims->total_tokens * dims->h_q, dims->head_dim,
+                                         dims->dtype == NSA_FP16, n_branch, o0, o1, o2, gates,
+                                         nullptr, dout, do0, do1, do2, dgates, true,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 nsa_status nsa_sel_attn_staging_size(const nsa_sel_attn_dims *dims, size_t *bytes) {

@@ -160,7 +160,8 @@ __device__ __forceinline__ void st_row_chunks(uint32_t tile, int row, int chunk0
 //     dS of its tile, the dQ epilogue (through its P/dS buffers, free once the dQ
 //     MMA has read them) and, at the end of a run, dK/dV out.
 // mbarriers hand each buffer between roles; every wait is bounded.
-template <int D, int BK, bool kFp16>
+// kWin: the sliding window's lower key bound is applied (p.window > 0).
+template <int D, int BK, bool kFp16, bool kWin>
 __global__ void __launch_bounds__(BwdCfg<D, BK>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
@@ -440,9 +441,12 @@ __global__ void __launch_bounds__(BwdCfg<D, BK>::kThreads, 1)
     TileSeq seq;
     seq.init(total, C);
     if (wg == 1) seq.next();
-    auto row_meta = [&](const TileDesc &d, int &lim, float &lse2, float &dval) {
+    // keys [lo, lim] of the block are visible to the row (lim < 0: no row): the causal
+    // limit and the start of a sliding window (0 without one)
+    auto row_meta = [&](const TileDesc &d, int &lim, int &lo, float &lse2, float &dval) {
       const int nrows = d.hn >> 16, h = d.hn & 0xffff;
       lim = -1;
+      lo = 0;
       lse2 = 0.f;
       dval = 0.f;
       if (row < nrows) {
@@ -450,14 +454,15 @@ __global__ void __launch_bounds__(BwdCfg<D, BK>::kThreads, 1)
         const int t = __ldg(p.q_list + d.q_off + rr / p.g);
         const int hq = h * p.g + rr % p.g;
         lim = min(BK - 1, t - d.key0);
+        if (kWin) lo = max(0, t - p.window + 1 - d.key0);
         lse2 = __ldg(p.lse_in + (int64_t)hq * p.n + t) * kLog2e;
         dval = __ldg(p.dstat + (int64_t)hq * p.n + t);
       }
     };
     TileDesc dsc = load_desc(p, seq);
-    int lim = -1;
+    int lim = -1, lo = 0;
     float lse2 = 0.f, dval = 0.f;
-    if (seq.valid()) row_meta(dsc, lim, lse2, dval);
+    if (seq.valid()) row_meta(dsc, lim, lo, lse2, dval);
     int dqw = 0;                                 // dQ halves this warpgroup has consumed
     for (int i = wg; seq.valid(); i += NWG) {
       const int tile = seq.tile();
@@ -479,7 +484,8 @@ __global__ void __launch_bounds__(BwdCfg<D, BK>::kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int ii = c * 32 + j;
-          float pr = (ii <= lim) ? ex2_approx(fmaf(sv[j], p.scale_log2, -lse2)) : 0.f;
+          float pr =
+              (ii <= lim && ii >= lo) ? ex2_approx(fmaf(sv[j], p.scale_log2, -lse2)) : 0.f;
           pr = round16<kFp16>(pr);
           sv[j] = pr;
           dp[j] = pr * (dp[j] - dval);
@@ -499,9 +505,9 @@ __global__ void __launch_bounds__(BwdCfg<D, BK>::kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&pds_full[wg]);
       // this warpgroup's next tile's row metadata: its loads overlap the MMAs and the epilogue
-      int nlim = -1;
+      int nlim = -1, nlo = 0;
       float nlse2 = 0.f, ndval = 0.f;
-      if (mseq.valid()) row_meta(mdsc, nlim, nlse2, ndval);
+      if (mseq.valid()) row_meta(mdsc, nlim, nlo, nlse2, ndval);
 
       // ---- dQ epilogue: TMEM -> 16 bits -> this warp's staging slots -> TMA
       //      stores.  The slots lie in this warpgroup's P buffer (and, with a single
@@ -581,6 +587,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BK>::kThreads, 1)
       seq = mseq;
       dsc = mdsc;
       lim = nlim;
+      lo = nlo;
       lse2 = nlse2;
       dval = ndval;
     }
@@ -708,13 +715,13 @@ static cudaError_t run_bwd(const Params &p, int num_sms, int64_t max_tiles, cuda
   bwd_parts_kernel<<<1, 1024, 0, stream>>>(p);
   mark(7, stream, false);
   const uint32_t smem = L::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D, BK, kFp16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = p.window > 0 ? bwd_main_kernel<D, BK, kFp16, true>
+                            : bwd_main_kernel<D, BK, kFp16, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   mark(8, stream, true);
-  bwd_main_kernel<D, BK, kFp16><<<static_cast<unsigned>(grid), L::kThreads, smem, stream>>>(
-      mk, mv, mdq, p);
+  kern<<<static_cast<unsigned>(grid), L::kThreads, smem, stream>>>(mk, mv, mdq, p);
   mark(8, stream, false);
   mark(9, stream, true);
   bwd_dq_kernel<D, kFp16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);

@@ -39,7 +39,7 @@ struct Layout {
   int64_t n_scan_ctas;     // CTAs of the sub-segment tile scan
   // index region
   size_t status, nb, blk_start, counts, offsets, tile_off, q_list, slot_map,
-      chunk_hist, npairs, cnt, prow, wtile_off, wscan_part, tdesc, tseg;
+      chunk_hist, npairs, prow, wtile_off, wscan_part, tdesc, tseg;
   size_t index_end;
   // forward scratch
   size_t obuf, mlbuf;
@@ -75,13 +75,14 @@ struct Params {
   float *lse;
   // workspace views
   int32_t *status, *nb, *blk_start, *counts, *offsets, *tile_off, *q_list,
-      *slot_map, *chunk_hist, *npairs, *cnt, *prow, *wtile_off, *wscan_part;
+      *slot_map, *chunk_hist, *npairs, *prow, *wtile_off, *wscan_part;
   TileDesc *tdesc;
   int32_t *tseg;    // (head, block) segment of every forward tile
   int64_t nb_max, n_idx_tiles, nsub, n_scan_ctas;
   int idx_tok, n_w, wave_tiles;
   int fwd_chunk;    // forward schedule: consecutive tiles per chunk, chunks dealt round-robin
   int bwd_chunk;    // the same for the backward main kernel
+  int window;       // sliding window: a row of token t sees keys >= t - window + 1 (0: none)
   void *obuf;       // forward partial outputs [tiles * 128, d] (dtype), tile-padded rows
   float2 *mlbuf;    // forward partial (max, sum) per padded row, log2 domain
   float *dstat;     // backward D = rowsum(dO * O) [h_q, N]

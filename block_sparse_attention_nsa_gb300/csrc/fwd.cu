@@ -81,7 +81,9 @@ constexpr int kFwdThreads = 512;
 //     staged one 64-column block at a time and written by TMA tensor stores to
 //     the tile's 128 rows of the compact buffer; (m, l) per row).
 // mbarriers hand each buffer between roles; every wait is bounded.
-template <int D, int BK, bool kFp16>
+// kWin: the sliding window's lower key bound is applied (p.window > 0); without it
+// the bound is compiled out.
+template <int D, int BK, bool kFp16, bool kWin>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_main_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -331,15 +333,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     TileSeq seq;
     seq.init(total, p.fwd_chunk);
     if (wg == 1) seq.next();
-    // descriptor and causal limit of this warpgroup's next tile, loaded one tile early
+    // descriptor and key range of this warpgroup's next tile, loaded one tile early:
+    // keys [lo, lim] of the block are visible to the row (lim < 0: no row); lim is the
+    // causal limit, lo the start of a sliding window (0 without one)
     auto tile_lim = [&](const TileDesc &d) {
       const int nrows = d.hn >> 16;
-      if (row >= nrows) return -1;
+      if (row >= nrows) return make_int2(-1, 0);
       const int t = __ldg(p.q_list + d.q_off + (d.row0 + row) / p.g);
-      return min(BK - 1, t - d.key0);
+      const int lo = kWin ? max(0, t - p.window + 1 - d.key0) : 0;
+      return make_int2(min(BK - 1, t - d.key0), lo);
     };
     TileDesc dsc = load_desc(p, seq);
-    int lim = seq.valid() ? tile_lim(dsc) : -1;
+    int2 lr = seq.valid() ? tile_lim(dsc) : make_int2(-1, 0);
+    int lim = lr.x, lo = lr.y;
     TileSeq nseq = seq;
     nseq.next();
     nseq.next();
@@ -365,7 +371,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tmem_ld32(tS + c * 32, sv);
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (c * 32 + j <= lim) mx = fmaxf(mx, sv[j]);
+            if (c * 32 + j <= lim && c * 32 + j >= lo) mx = fmaxf(mx, sv[j]);
         }
         m2 = row_in ? mx * p.scale_log2 : 0.f;
 #pragma unroll
@@ -376,8 +382,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             const int ii = c * 32 + j;
-            const float p0 = (ii <= lim) ? ex2_approx(fmaf(sv[j], p.scale_log2, -m2)) : 0.f;
-            const float p1 = (ii + 1 <= lim) ? ex2_approx(fmaf(sv[j + 1], p.scale_log2, -m2)) : 0.f;
+            const float p0 =
+                (ii <= lim && ii >= lo) ? ex2_approx(fmaf(sv[j], p.scale_log2, -m2)) : 0.f;
+            const float p1 = (ii + 1 <= lim && ii + 1 >= lo)
+                                 ? ex2_approx(fmaf(sv[j + 1], p.scale_log2, -m2))
+                                 : 0.f;
             lsum += p0 + p1;                    // fp32 row sum (exact lse)
             pk[j / 2] = pack2<kFp16>(p0, p1);   // P rounded to 16 bits for the PV MMA
           }
@@ -393,10 +402,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         } else {
           tmem_ld32(tS, sv);
         }
-        // Only rows of a tile of the token's own block need the causal mask; a
-        // warp whose rows all see the whole block takes the unmasked path.
-        // Eight independent max / sum chains keep the dependent latency short.
-        const bool full = __all_sync(0xffffffffu, !row_in || lim >= BK - 1);
+        // Only rows of a tile of the token's own block (or of a window's first block)
+        // need a mask; a warp whose rows all see the whole block takes the unmasked
+        // path.  Eight independent max / sum chains keep the dependent latency short.
+        const bool full = __all_sync(0xffffffffu, !row_in || (lim >= BK - 1 && lo <= 0));
         float mxs[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) mxs[j] = -INFINITY;
@@ -406,7 +415,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         } else {
 #pragma unroll
           for (int j = 0; j < BK; ++j)
-            if (j <= lim) mxs[j & 7] = fmaxf(mxs[j & 7], sv[j]);
+            if (j <= lim && j >= lo) mxs[j & 7] = fmaxf(mxs[j & 7], sv[j]);
         }
         const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
                                fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
@@ -423,8 +432,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             float p0 = ex2_approx(fmaf(sv[ii], p.scale_log2, -m2));
             float p1 = ex2_approx(fmaf(sv[ii + 1], p.scale_log2, -m2));
             if (!full) {
-              p0 = (ii <= lim) ? p0 : 0.f;
-              p1 = (ii + 1 <= lim) ? p1 : 0.f;
+              p0 = (ii <= lim && ii >= lo) ? p0 : 0.f;
+              p1 = (ii + 1 <= lim && ii + 1 >= lo) ? p1 : 0.f;
             }
             ls[(j >> 1) & 7] += p0 + p1;        // fp32 row sum (exact lse)
             pk[j / 2] = pack2<kFp16>(p0, p1);   // P rounded to 16 bits for the PV MMA
@@ -436,8 +445,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[i & 1]);
-      // the next tile's causal limit: its q_list read overlaps this epilogue
-      const int nlim = nseq.valid() ? tile_lim(ndsc) : -1;
+      // the next tile's key range: its q_list read overlaps this epilogue
+      const int2 nlr = nseq.valid() ? tile_lim(ndsc) : make_int2(-1, 0);
 
       // epilogue: O(i) -> 16-bit, one 64-column block at a time; each warp stages
       // its 32 rows in its own slots and TMA-stores them to the tile's
@@ -483,7 +492,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       st_global_v2_hint(p.mlbuf + (int64_t)tile * kTileRows + row, make_float2(m2, lsum), stream);
       seq = nseq;
       dsc = ndsc;
-      lim = nlim;
+      lim = nlr.x;
+      lo = nlr.y;
       nseq.next();
       nseq.next();
       ndsc = load_desc(p, nseq);
@@ -649,15 +659,15 @@ static cudaError_t run_fwd(const Params &p, int num_sms, int64_t max_tiles, cuda
     return cudaErrorInvalidValue;
   // One CTA per SM: it owns all 512 TMEM columns.
   const uint32_t smem = L::kBytes > 120u * 1024u ? L::kBytes : 120u * 1024u;
-  cudaError_t e = cudaFuncSetAttribute(fwd_main_kernel<D, BK, kFp16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = p.window > 0 ? fwd_main_kernel<D, BK, kFp16, true>
+                            : fwd_main_kernel<D, BK, kFp16, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   int64_t grid = num_sms;
   if (grid > max_tiles) grid = max_tiles > 0 ? max_tiles : 1;
   mark(5, stream, true);
-  fwd_main_kernel<D, BK, kFp16>
-      <<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, mo, p);
+  kern<<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, mo, p);
   mark(5, stream, false);
   const int64_t rows = static_cast<int64_t>(p.n) * p.h_q;
   mark(6, stream, true);

@@ -211,6 +211,54 @@ NSA_API nsa_status nsa_sel_attn_fwd_noalloc_status(const nsa_sel_attn_dims *dims
  * chip.  Asynchronous on `stream`; q, caches and out 16-byte aligned.  The pages give
  * no decode algorithm; this entry point is the forward restricted to one token per
  * sequence. */
+/* Sliding-window branch (the third of Native Sparse Attention's parallel branches: the
+ * papernotes page's 领域现状; window_size = 512 in the Flash-Sparse-Attention README's
+ * "Usage").  A token at local position tau attends to the keys of (tau - window,
+ * tau] of its sequence, causal, one softmax.  It runs on the selected-attention
+ * kernels:
+ *   nsa_sel_attn_window_select writes the selection rows of the window: int32
+ *     [h_k, N, topk], the blocks holding those keys, newest first (c(t), c(t) - 1,
+ *     ...), the other slots -1.  topk must be at least ceil((window - 1) / B_K) + 1,
+ *     else NSA_ERR_INVALID_ARG.
+ *   nsa_sel_attn_fwd_window and nsa_sel_attn_bwd_window are nsa_sel_attn_fwd and
+ *     nsa_sel_attn_bwd with the window's lower key bound added to the causal mask
+ *     (window >= 1).  Given a window selection, they compute sliding-window
+ *     attention.  Given any other selection, they compute that selection restricted
+ *     to the window.  Arguments, workspace and errors are those of fwd and bwd. */
+NSA_API nsa_status nsa_sel_attn_window_select(const nsa_sel_attn_dims *dims,
+                                              const int32_t *cu_seqlens, int window,
+                                              int32_t *sel_idx, nsa_stream_t stream);
+NSA_API nsa_status nsa_sel_attn_fwd_window(const nsa_sel_attn_dims *dims, const void *q,
+                                           const void *k, const void *v, const int32_t *sel_idx,
+                                           const int32_t *cu_seqlens, float scale, int window,
+                                           void *out, float *lse, void *workspace,
+                                           size_t workspace_bytes, nsa_stream_t stream);
+NSA_API nsa_status nsa_sel_attn_bwd_window(const nsa_sel_attn_dims *dims, const void *q,
+                                           const void *k, const void *v, const int32_t *sel_idx,
+                                           const int32_t *cu_seqlens, float scale, int window,
+                                           const void *out, const float *lse, const void *dout,
+                                           void *dq, void *dk, void *dv, void *workspace,
+                                           size_t workspace_bytes, int index_ready,
+                                           nsa_stream_t stream);
+
+/* Gated combination of the branch outputs: out[t, hq] = sum_b gates[t, hq, b] * o_b[t,
+ * hq] for n_branch = 1..3 branches o0, o1, o2, each [N, h_q, d] (dtype).
+ *   gates: float32 [N, h_q, n_branch], the gate values, e.g. sigmoids of a gate
+ *     projection.  The projection itself belongs to the model, not to this library.
+ *   Backward: d o_b = gates[., b] * dout, and dgates[., b] = sum_d dout * o_b
+ *     (fp32).  A NULL do_b skips that branch's output gradient.
+ * dims supplies N, h_q, head_dim and dtype.  The branch pointers must be 4-byte
+ * aligned.  The pages name the gated three-branch output but give no formula beyond
+ * the weighted sum. */
+NSA_API nsa_status nsa_gate_combine_fwd(const nsa_sel_attn_dims *dims, int n_branch,
+                                        const void *o0, const void *o1, const void *o2,
+                                        const float *gates, void *out, nsa_stream_t stream);
+NSA_API nsa_status nsa_gate_combine_bwd(const nsa_sel_attn_dims *dims, int n_branch,
+                                        const void *o0, const void *o1, const void *o2,
+                                        const float *gates, const void *dout, void *do0,
+                                        void *do1, void *do2, float *dgates,
+                                        nsa_stream_t stream);
+
 NSA_API nsa_status nsa_sel_attn_decode(const nsa_sel_attn_dims *dims, const void *q,
                                        const void *k_cache, const void *v_cache,
                                        const int32_t *sel_idx, const int32_t *cu_seqlens,
