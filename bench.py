@@ -422,6 +422,57 @@ def extended_sweep(torch, dev, pk_burst):
         del rr
         torch.cuda.empty_cache()
     outd.update(decode_sweep(torch, dev))
+    outd.update(window_sweep(torch, dev, pk_burst))
+    return outd
+
+
+def window_sweep(torch, dev, pk_burst):
+    """Sliding-window branch (window 512) on the 64K workload's shape, g = 4, and the
+    gated combination of three branch outputs of that shape."""
+    import dataclasses
+    import block_sparse_attention_nsa_gb300 as nsa
+    from workloads import CONFIGS, make_inputs
+    W, blk = 512, 64
+    topk = (W - 1 + blk - 1) // blk + 1
+    c = dataclasses.replace(CONFIGS["fwd64k"].with_g(4), topk=topk, name="window64k_g4")
+    inp = make_inputs(c, with_dout=True)
+    q, k, v, do = (inp[x].to(dev) for x in ("q", "k", "v", "dout"))
+    cu = torch.from_numpy(inp["cu_seqlens"]).to(dev)
+    sel = nsa.window_select(cu, c.n, c.h_k, blk, topk, W)
+    ws = nsa.alloc_workspace(nsa.make_dims(1, c.n, c.h_q, c.h_k, c.d, blk, topk, q.dtype), dev)
+    state = {}
+
+    def fwd():
+        state["o"] = nsa.fwd_window(q, k, v, sel, cu, blk, c.scale, W, workspace=ws)
+
+    def bwd():
+        o, l = state["o"]
+        nsa.bwd_window(q, k, v, sel, cu, blk, c.scale, W, o, l, do, workspace=ws,
+                       index_ready=True)
+    fwd()
+    bwd()
+    torch.cuda.synchronize()
+    f_ms = dist(time_reps(torch, fwd, 20))["median"]
+    fwd()
+    b_ms = dist(time_reps(torch, bwd, 20))["median"]
+    keys = float(np.minimum(np.arange(c.n) + 1, W).sum())          # one 64K sequence
+    ff = 4.0 * c.d * c.h_q * keys
+    outd = {"window64k_w512_g4": {"fwd_ms": f_ms, "bwd_ms": b_ms,
+                                  "fwd_tflops": ff / (f_ms * 1e-3) / 1e12,
+                                  "bwd_tflops": 2.5 * ff / (b_ms * 1e-3) / 1e12,
+                                  "fwd_pct_peak": 100 * ff / (f_ms * 1e-3) / 1e12 / pk_burst}}
+    o = state["o"][0]
+    branches = [o, o.clone(), o.clone()]
+    gates = torch.rand(c.n, c.h_q, 3, device=dev)
+    comb = lambda: nsa.gate_combine(branches, gates)
+    comb()
+    ms = dist(time_reps(torch, comb, 20))["median"]
+    nbytes = 4 * o.numel() * o.element_size() + gates.numel() * 4
+    outd["gate_combine_3x64k_g4"] = {"us": ms * 1e3, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+                                     "frac_of_measured_hbm": nbytes / (ms * 1e-3) / 1e9 /
+                                     peaks()[2]}
+    del ws, q, k, v, do
+    torch.cuda.empty_cache()
     return outd
 
 
