@@ -165,8 +165,7 @@ NSA_API nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const v
  *     NSA_NOALLOC_SCRATCH_BYTES are rejected with NSA_ERR_WORKSPACE; nothing runs.
  *   - The first call on a device looks up the array's device address (with that
  *     device current) and keeps it; the lookup is repeated when the device's
- *     current context has changed (after cudaDeviceReset, for instance).  Make the
- *     first call in each context before any stream capture.
+ *     current context has changed (after cudaDeviceReset, for instance).
  *   - All calls share the one array and it keeps the last call's contents: calls
  *     that may overlap on the GPU (different streams without ordering, several
  *     host threads) race; serialise them.  The call clears the status word itself
