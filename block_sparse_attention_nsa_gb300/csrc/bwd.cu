@@ -130,6 +130,18 @@ struct BwdCfg {
   static_assert(!kDqAlias || DQC <= 2 * BK, "aliased dQ fits the S/dP columns");
 };
 
+// 32 values of a row, already packed in 16-bit pairs, into four 16-byte chunks of a
+// 128-byte-swizzled operand tile
+__device__ __forceinline__ void st_row_packed(uint32_t tile, int row, int chunk0, const uint32_t *pk) {
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const uint32_t so = sw128_offset(row, chunk0 + q4, 128);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tile + so), "r"(pk[q4 * 4]),
+                 "r"(pk[q4 * 4 + 1]), "r"(pk[q4 * 4 + 2]), "r"(pk[q4 * 4 + 3])
+                 : "memory");
+  }
+}
+
 template <bool kFp16>
 __device__ __forceinline__ void st_row_chunks(uint32_t tile, int row, int chunk0, const float *v32) {
   uint32_t pk[16];
@@ -476,22 +488,31 @@ __global__ void __launch_bounds__(BwdCfg<D, BK>::kThreads, 1)
       mbar_wait_sticky(&sdp_full[wg], (i / NWG) & 1, p.status, &fail);
       tc_fence_after();
       // ---- P and dS of this row, written in 16 bits as MMA operands ----
+      // A warp whose rows all see the whole block skips the mask.  Rows past the
+      // tile's end take that path too: their Q and dO rows are zero, so they add
+      // nothing to dV, dK or a dQ row anyone reads.  dS uses the 16-bit P the MMAs see.
+      const bool full = __all_sync(0xffffffffu, lim < 0 || (lim >= BK - 1 && lo <= 0));
 #pragma unroll
       for (int c = 0; c < BK / 32; ++c) {
         float sv[32], dp[32];
         tmem_ld32(tS + lane_off + c * 32, sv);
         tmem_ld32(tDP + lane_off + c * 32, dp);
+        uint32_t pp[16], dd[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 32; j += 2) {
           const int ii = c * 32 + j;
-          float pr =
-              (ii <= lim && ii >= lo) ? ex2_approx(fmaf(sv[j], p.scale_log2, -lse2)) : 0.f;
-          pr = round16<kFp16>(pr);
-          sv[j] = pr;
-          dp[j] = pr * (dp[j] - dval);
+          float p0 = ex2_approx(fmaf(sv[j], p.scale_log2, -lse2));
+          float p1 = ex2_approx(fmaf(sv[j + 1], p.scale_log2, -lse2));
+          if (!full) {
+            p0 = (ii <= lim && ii >= lo) ? p0 : 0.f;
+            p1 = (ii + 1 <= lim && ii + 1 >= lo) ? p1 : 0.f;
+          }
+          pp[j / 2] = pack2<kFp16>(p0, p1);
+          const float2 pr = unpack2<kFp16>(pp[j / 2]);
+          dd[j / 2] = pack2<kFp16>(pr.x * (dp[j] - dval), pr.y * (dp[j + 1] - dval));
         }
-        st_row_chunks<kFp16>(sP, row, c * 4, sv);
-        st_row_chunks<kFp16>(sDS, row, c * 4, dp);
+        st_row_packed(sP, row, c * 4, pp);
+        st_row_packed(sDS, row, c * 4, dd);
       }
       if constexpr (BK < 64) {   // zero the unused half of the swizzle atom read by N = 64
         float z[32];
