@@ -24,27 +24,53 @@
 namespace nsa {
 
 // ---------------------------------------------------------------------------
-// D = rowsum(dO * O): one warp per (token, query head)
+// D = rowsum(dO * O): one warp per four (token, query head) rows
 // ---------------------------------------------------------------------------
 template <int D, bool kFp16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(Params p) {
-  constexpr int E = D / 32;
+  // four rows per warp, their loads issued together
+  constexpr int E = D / 32, R = 4;
   const int lane = threadIdx.x & 31;
-  const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (wid >= (int64_t)p.n * p.h_q) return;
-  const int t = static_cast<int>(wid / p.h_q), hq = static_cast<int>(wid - (int64_t)t * p.h_q);
-  const uint16_t *o = static_cast<const uint16_t *>(p.out_in) + wid * D + lane * E;
-  const uint16_t *g = static_cast<const uint16_t *>(p.dout) + wid * D + lane * E;
-  float acc = 0.f;
+  const int64_t rows = (int64_t)p.n * p.h_q;
+  const int64_t r0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * R;
+  if (r0 >= rows) return;
+  uint32_t a[R][E / 2], b[R][E / 2];
 #pragma unroll
-  for (int e = 0; e < E; e += 2) {
-    const float2 a = unpack2<kFp16>(*reinterpret_cast<const uint32_t *>(o + e));
-    const float2 b = unpack2<kFp16>(*reinterpret_cast<const uint32_t *>(g + e));
-    acc = fmaf(a.x, b.x, fmaf(a.y, b.y, acc));
+  for (int k = 0; k < R; ++k) {
+    const int64_t r = min(r0 + k, rows - 1);
+    const uint16_t *o = static_cast<const uint16_t *>(p.out_in) + r * D + lane * E;
+    const uint16_t *g = static_cast<const uint16_t *>(p.dout) + r * D + lane * E;
+    if constexpr (E == 2) {
+      a[k][0] = __ldcs(reinterpret_cast<const unsigned int *>(o));
+      b[k][0] = __ldcs(reinterpret_cast<const unsigned int *>(g));
+    } else if constexpr (E == 4) {
+      const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(o));
+      const uint2 y = __ldcs(reinterpret_cast<const uint2 *>(g));
+      a[k][0] = x.x; a[k][1] = x.y; b[k][0] = y.x; b[k][1] = y.y;
+    } else {
+      const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(o));
+      const uint4 y = __ldcs(reinterpret_cast<const uint4 *>(g));
+      a[k][0] = x.x; a[k][1] = x.y; a[k][2] = x.z; a[k][3] = x.w;
+      b[k][0] = y.x; b[k][1] = y.y; b[k][2] = y.z; b[k][3] = y.w;
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) p.dstat[(int64_t)hq * p.n + t] = acc;
+  for (int k = 0; k < R; ++k) {
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < E / 2; ++e) {
+      const float2 x = unpack2<kFp16>(a[k][e]);
+      const float2 y = unpack2<kFp16>(b[k][e]);
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const int64_t r = r0 + k;
+    if (lane == 0 && r < rows) {
+      const int t = static_cast<int>(r / p.h_q), hq = static_cast<int>(r - (int64_t)t * p.h_q);
+      p.dstat[(int64_t)hq * p.n + t] = acc;
+    }
+  }
 }
 
 // First dK/dV partial slot of every segment.  The main kernel deals tiles in
@@ -732,7 +758,7 @@ static cudaError_t run_bwd(const Params &p, int num_sms, int64_t max_tiles, cuda
   const int64_t rows = static_cast<int64_t>(p.n) * p.h_q;
   int grid = num_sms < kMaxBwdCtas ? num_sms : kMaxBwdCtas;
   mark(7, stream, true);
-  bwd_pre_kernel<D, kFp16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+  bwd_pre_kernel<D, kFp16><<<static_cast<unsigned>((rows + 31) / 32), 256, 0, stream>>>(p);
   bwd_parts_kernel<<<1, 1024, 0, stream>>>(p);
   mark(7, stream, false);
   const uint32_t smem = L::kBytes;
