@@ -108,13 +108,15 @@ nsa_status check_dims(const nsa_sel_attn_dims *d, bool bwd) {
 // the CTAs, so that all CTAs work on neighbouring (head, block) segments at any
 // time and the Q rows and K/V blocks they read stay L2-resident.
 #ifndef NSA_FWD_CHUNK
-#define NSA_FWD_CHUNK 8
+#define NSA_FWD_CHUNK 4
 #endif
 constexpr int kFwdChunk = NSA_FWD_CHUNK;
 // Backward schedule: the same dealing; the backward also writes one dK/dV partial per
-// (segment, chunk) pair, so longer chunks mean fewer partials.
+// (segment, chunk) pair, so longer chunks mean fewer partials.  Chunk lengths measured
+// on the 64K workload (forward 2/4/8/16, backward 8/16/32/64): 4 and 32 give the
+// shortest forward + backward step at g = 4.
 #ifndef NSA_BWD_CHUNK
-#define NSA_BWD_CHUNK 16
+#define NSA_BWD_CHUNK 32
 #endif
 constexpr int kBwdChunk = NSA_BWD_CHUNK;
 
