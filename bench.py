@@ -33,9 +33,9 @@ DOMINANT = ("fwd_main", "bwd_main")
 # kernels on the 64K workload, from one ncu capture of the kernel sources whose
 # SHA-256 is given (profiles/dram_traffic_fwd64k_g4.md).  Reported only while the
 # sources are unchanged; otherwise the roofline's traffic is null.
-TRAFFIC = {"sources_sha256": "8396e0b670b0ed4f44a6e3d00ee14924a6579ffaf73e6aefb6da326a758f100a",
-           "bytes": {"fwd_main": {"4": 925940224 + 4403137280},
-                     "bwd_main": {"4": 2769964800 + 5059977472}}}
+TRAFFIC = {"sources_sha256": "c5478fdc15b4a1d498d022992736a416f7341be0c3cad5fd82635c892dd966c5",
+           "bytes": {"fwd_main": {"4": 925593088 + 4402661632},
+                     "bwd_main": {"4": 2847239680 + 4798372864}}}
 
 
 def kernel_sources_hash() -> str:
