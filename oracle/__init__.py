@@ -22,6 +22,10 @@ Parity status per function (pins live in tests/test_oracle_*.py):
                     >= sequence length equals plain causal attention.
   gate_combine / gate_combine_bwd -- pinned: closed-form sums and central finite
                     differences of the gates.
+  compress (module oracle.compress, numpy fp64) -- compression, compressed
+                    attention, block importance and top-T selection; pinned: closed
+                    forms, torch SDPA with an explicit mask, l = stride = 1 equals
+                    causal attention, key-level and sort-based brute force.
 """
 from __future__ import annotations
 
