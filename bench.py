@@ -423,6 +423,7 @@ def extended_sweep(torch, dev, pk_burst):
         torch.cuda.empty_cache()
     outd.update(decode_sweep(torch, dev))
     outd.update(window_sweep(torch, dev, pk_burst))
+    outd.update(cmp_sweep(torch, dev, pk_burst))
     return outd
 
 
@@ -473,6 +474,46 @@ def window_sweep(torch, dev, pk_burst):
                                      peaks()[2]}
     del ws, q, k, v, do
     torch.cuda.empty_cache()
+    return outd
+
+
+def cmp_sweep(torch, dev, pk_burst):
+    """The step before selected attention on the 64K workload's shape (h_k = 4, d = 128,
+    g = 1 and 4): compression (kernel_size 32, stride 16), then compressed attention
+    with block importance and top-16 selection (B_K = 64, 1 init and 2 local blocks).
+    Useful FLOPs are QK^T and PV over the visible compressed tokens; the kernel also
+    recomputes QK^T once to form the exact probabilities for the importance."""
+    import block_sparse_attention_nsa_gb300 as nsa
+    from workloads import CONFIGS, make_inputs
+    outd = {}
+    for g in (1, 4):
+        c = CONFIGS["fwd64k"].with_g(g)
+        inp = make_inputs(c)
+        q, k, v = (inp[x].to(dev) for x in ("q", "k", "v"))
+        cu = torch.from_numpy(inp["cu_seqlens"]).to(dev)
+        state = {}
+
+        def comp():
+            state["c"] = nsa.compress_kv(k, v, cu, 32, 16)
+
+        def sel():
+            kc, vc, cc = state["c"]
+            nsa.cmp_attn_select(q, kc, vc, cu, cc, 32, 16, c.n, c.scale, 64, 16, 1, 2)
+        comp()
+        sel()
+        torch.cuda.synchronize()
+        c_ms = dist(time_reps(torch, comp, 20))["median"]
+        s_ms = dist(time_reps(torch, sel, 10))["median"]
+        tau = np.arange(c.n)
+        nv = float(np.where(tau >= 31, (tau - 31) // 16 + 1, 0).sum())
+        ff = 4.0 * c.d * c.h_q * nv
+        outd[f"cmp_select_64k_g{g}"] = {
+            "compress_ms": c_ms, "attn_select_ms": s_ms,
+            "useful_tflops": ff / (s_ms * 1e-3) / 1e12,
+            "issued_tflops": 1.5 * ff / (s_ms * 1e-3) / 1e12,
+            "pct_peak_issued": 100 * 1.5 * ff / (s_ms * 1e-3) / 1e12 / pk_burst}
+        del q, k, v, state
+        torch.cuda.empty_cache()
     return outd
 
 

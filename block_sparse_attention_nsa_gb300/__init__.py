@@ -19,7 +19,7 @@ import torch
 
 __all__ = ["Dims", "NsaError", "load", "workspace_size", "index", "index_view", "fwd", "bwd",
            "decode", "window_select", "fwd_window", "bwd_window", "gate_combine",
-           "gate_combine_bwd",
+           "gate_combine_bwd", "compress_kv", "cmp_attn_select",
            "staging_size", "step_host", "get_status", "profile_enable", "profile_collect",
            "kernel_names", "make_dims", "LIB_PATH"]
 
@@ -81,6 +81,11 @@ def load():
         "nsa_gate_combine_fwd": (st, [dp, ctypes.c_int, vp, vp, vp, vp, vp, vp]),
         "nsa_gate_combine_bwd": (st, [dp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                       vp]),
+        "nsa_compress_kv": (st, [dp, vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp,
+                                 vp]),
+        "nsa_cmp_attn_select": (st, [dp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, f32, ctypes.c_int, ctypes.c_int, vp, vp, vp,
+                                     vp, vp]),
         "nsa_sel_attn_num_kernels": (i32, []),
         "nsa_sel_attn_kernel_name": (ctypes.c_char_p, [i32]),
         "nsa_sel_attn_profile_enable": (st, [i32]),
@@ -249,6 +254,45 @@ def decode(q, k_cache, v_cache, sel_idx, cu_seqlens, block_size: int, scale: flo
         _ptr(cu_seqlens), float(scale), _ptr(out), _ptr(lse), _ptr(device_status),
         _stream(stream)), "decode")
     return out, lse
+
+
+def compress_kv(k, v, cu_seqlens, kernel_size: int, kernel_stride: int, device_status=None,
+                stream=None):
+    """Compressed keys and values: kc, vc [N // kernel_stride, h_k, d] (rows past the
+    total are unused) and cu_cmp int32 [S + 1], each sequence's compressed rows."""
+    _contig(k, v, cu_seqlens)
+    n, h_k, d = k.shape
+    dims = make_dims(cu_seqlens.numel() - 1, n, h_k, h_k, d, 64, 1, k.dtype)
+    rows = n // kernel_stride
+    kc = torch.empty((rows, h_k, d), dtype=k.dtype, device=k.device)
+    vc = torch.empty_like(kc)
+    cu_cmp = torch.empty(cu_seqlens.numel(), dtype=torch.int32, device=k.device)
+    _check(load().nsa_compress_kv(ctypes.byref(dims), _ptr(cu_seqlens), int(kernel_size),
+                                  int(kernel_stride), _ptr(k), _ptr(v), _ptr(kc), _ptr(vc),
+                                  _ptr(cu_cmp), _ptr(device_status), _stream(stream)),
+           "compress_kv")
+    return kc, vc, cu_cmp
+
+
+def cmp_attn_select(q, kc, vc, cu_seqlens, cu_cmp, kernel_size: int, kernel_stride: int,
+                    max_seqlen: int, scale: float, block_size: int, topk: int,
+                    init_blocks: int = 1, local_blocks: int = 2, device_status=None,
+                    stream=None):
+    """Compressed attention and top-T block selection: out [N, h_q, d], lse float32
+    [h_q, N] and sel_idx int32 [h_k, N, topk]."""
+    _contig(q, kc, vc, cu_seqlens, cu_cmp)
+    n, h_q, d = q.shape
+    h_k = kc.shape[1]
+    dims = make_dims(cu_seqlens.numel() - 1, n, h_q, h_k, d, block_size, topk, q.dtype)
+    out = torch.empty_like(q)
+    lse = torch.empty((h_q, n), dtype=torch.float32, device=q.device)
+    sel = torch.empty((h_k, n, topk), dtype=torch.int32, device=q.device)
+    _check(load().nsa_cmp_attn_select(
+        ctypes.byref(dims), _ptr(q), _ptr(kc), _ptr(vc), _ptr(cu_seqlens), _ptr(cu_cmp),
+        int(kernel_size), int(kernel_stride), int(max_seqlen), float(scale), int(init_blocks),
+        int(local_blocks), _ptr(out), _ptr(lse), _ptr(sel), _ptr(device_status),
+        _stream(stream)), "cmp_attn_select")
+    return out, lse, sel
 
 
 def window_select(cu_seqlens, total_tokens: int, h_k: int, block_size: int, topk: int,

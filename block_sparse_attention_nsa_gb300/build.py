@@ -12,7 +12,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnsa_sel.so")
-SOURCES = ["api.cu", "index_build.cu", "fwd.cu", "bwd.cu", "noalloc.cu", "decode.cu", "window.cu"]
+SOURCES = ["api.cu", "index_build.cu", "fwd.cu", "bwd.cu", "noalloc.cu", "decode.cu", "window.cu",
+           "compress.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -24,6 +24,14 @@ cudaError_t launch_decode(int num_seqs, int h_q, int h_k, int d, int block, int 
                           int32_t *status, cudaStream_t s);
 cudaError_t launch_bwd(const Params &p, int num_sms, int64_t max_tiles, cudaStream_t s,
                        void (*mark)(int, cudaStream_t, bool));
+cudaError_t launch_cmp_offsets(const int32_t *cu, int num_seqs, int n, int ksize, int stride,
+                               int32_t *cu_cmp, int32_t *status, cudaStream_t s);
+cudaError_t launch_compress(int d, bool fp16, const int32_t *cu, const int32_t *cu_cmp,
+                            int num_seqs, int n, int h_k, int ksize, int stride,
+                            int64_t rows_cap, const void *k, const void *v, void *kc, void *vc,
+                            cudaStream_t s);
+cudaError_t launch_cmp_select(int d, bool fp16, const CmpParams &p, cudaStream_t s);
+int cmp_tokens_per_cta(int d, int g, int nb_max);
 
 namespace {
 
@@ -622,6 +630,88 @@ nsa_status nsa_sel_attn_decode(const nsa_sel_attn_dims *dims, const void *q, con
                                    dims->block_size, dims->topk, dims->dtype == NSA_FP16, scale,
                                    q, k_cache, v_cache, sel_idx, cu_seqlens, out, lse,
                                    device_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static nsa_status check_cmp(const nsa_sel_attn_dims *dims, int kernel_size, int kernel_stride) {
+  nsa_status st = check_dims(dims, false);
+  if (st != NSA_OK) return st;
+  if (!(dims->head_dim == 64 || dims->head_dim == 128)) return NSA_ERR_UNSUPPORTED;
+  if (kernel_stride < 1 || kernel_size < kernel_stride) return NSA_ERR_INVALID_ARG;
+  if (dims->h_q / dims->h_k > 128) return NSA_ERR_UNSUPPORTED;
+  return NSA_OK;
+}
+
+nsa_status nsa_compress_kv(const nsa_sel_attn_dims *dims, const int32_t *cu_seqlens,
+                           int kernel_size, int kernel_stride, const void *k, const void *v,
+                           void *kc, void *vc, int32_t *cu_cmp, int32_t *device_status,
+                           nsa_stream_t stream) {
+  nsa_status st = check_cmp(dims, kernel_size, kernel_stride);
+  if (st != NSA_OK) return st;
+  const int64_t rows_cap = dims->total_tokens / kernel_stride;
+  if (!cu_seqlens || !cu_cmp) return NSA_ERR_INVALID_ARG;
+  if (rows_cap > 0 && (!k || !v || !kc || !vc)) return NSA_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(kc, 16) || !aligned(vc, 16) ||
+      !aligned(cu_cmp, 4) || (device_status && !aligned(device_status, 4)))
+    return NSA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_cmp_offsets(cu_seqlens, dims->num_seqs, dims->total_tokens, kernel_size,
+                                     kernel_stride, cu_cmp, device_status, s);
+  if (e != cudaSuccess) return NSA_ERR_CUDA;
+  return cuda_status(launch_compress(dims->head_dim, dims->dtype == NSA_FP16, cu_seqlens, cu_cmp,
+                                     dims->num_seqs, dims->total_tokens, dims->h_k, kernel_size,
+                                     kernel_stride, rows_cap, k, v, kc, vc, s));
+}
+
+nsa_status nsa_cmp_attn_select(const nsa_sel_attn_dims *dims, const void *q, const void *kc,
+                               const void *vc, const int32_t *cu_seqlens, const int32_t *cu_cmp,
+                               int kernel_size, int kernel_stride, int max_seqlen, float scale,
+                               int init_blocks, int local_blocks, void *out, float *lse,
+                               int32_t *sel_idx, int32_t *device_status, nsa_stream_t stream) {
+  nsa_status st = check_cmp(dims, kernel_size, kernel_stride);
+  if (st != NSA_OK) return st;
+  if (max_seqlen < 1 || init_blocks < 0 || local_blocks < 0 || !(scale > 0.f))
+    return NSA_ERR_INVALID_ARG;
+  if (!cu_seqlens || !cu_cmp) return NSA_ERR_INVALID_ARG;
+  if (dims->total_tokens > 0 && (!q || !out || !lse || !sel_idx)) return NSA_ERR_INVALID_ARG;
+  const int64_t rows_cap = dims->total_tokens / kernel_stride;
+  if (rows_cap > 0 && (!kc || !vc)) return NSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kc, 16) || !aligned(vc, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(sel_idx, 4) || (device_status && !aligned(device_status, 4)))
+    return NSA_ERR_INVALID_ARG;
+  const int g = dims->h_q / dims->h_k;
+  const int64_t nb_max = ((int64_t)max_seqlen + dims->block_size - 1) / dims->block_size;
+  if (nb_max > (int64_t(1) << 20)) return NSA_ERR_UNSUPPORTED;
+  const int tt = cmp_tokens_per_cta(dims->head_dim, g, static_cast<int>(nb_max));
+  if (tt == 0) return NSA_ERR_UNSUPPORTED;
+  CmpParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.kc = kc;
+  p.vc = vc;
+  p.cu = cu_seqlens;
+  p.cu_cmp = cu_cmp;
+  p.num_seqs = dims->num_seqs;
+  p.n = dims->total_tokens;
+  p.h_q = dims->h_q;
+  p.h_k = dims->h_k;
+  p.g = g;
+  p.ksize = kernel_size;
+  p.stride = kernel_stride;
+  p.block = dims->block_size;
+  p.topk = dims->topk;
+  p.init_blocks = init_blocks;
+  p.local_blocks = local_blocks;
+  p.max_seqlen = max_seqlen;
+  p.tt = tt;
+  p.nb_max = static_cast<int>(nb_max);
+  p.rows_cap = rows_cap;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out = out;
+  p.lse = lse;
+  p.sel = sel_idx;
+  p.status = device_status;
+  return cuda_status(launch_cmp_select(dims->head_dim, dims->dtype == NSA_FP16, p,
+                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 nsa_status nsa_sel_attn_get_status(const nsa_sel_attn_dims *dims, void *workspace,

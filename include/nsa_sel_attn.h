@@ -258,6 +258,56 @@ NSA_API nsa_status nsa_gate_combine_bwd(const nsa_sel_attn_dims *dims, int n_bra
                                         void *do1, void *do2, float *dgates,
                                         nsa_stream_t stream);
 
+/* The step before selected attention: the compressed branch and the top-T block
+ * selection that produce sel_idx (Native Sparse Attention's compression and selection
+ * branches, papernotes page, 研究背景与动机 "领域现状" and the 方法详解 flowchart's
+ * selection tensor T; kernel_size 32, kernel_stride 16, block_size 64, topk 16,
+ * init_blocks 1 and local_blocks 2 in the Flash-Sparse-Attention README's "Usage").
+ * The pages give no formula for these steps; the library takes these readings:
+ *   compression: compressed token i of a sequence is the mean of the keys (values)
+ *     at positions [i*stride, i*stride + kernel_size); it exists when that window
+ *     lies inside the sequence;
+ *   the query at position tau (within its sequence) sees compressed token i when
+ *     i*stride + kernel_size - 1 <= tau;
+ *   compressed attention: out = softmax(scale * q . kc) vc over the visible
+ *     compressed tokens, lse its log-sum-exp; no visible token: out 0, lse -inf;
+ *   importance of block j (keys [j*B_K, j*B_K + B_K)) for a (KV head, token): the
+ *     sum, over the group's g query heads and the visible compressed tokens whose
+ *     window overlaps those keys, of the compressed-attention probability;
+ *   selection: among the causal blocks j <= tau / B_K, first the init blocks
+ *     (j < init_blocks) and the local blocks (tau/B_K - local_blocks < j), ascending,
+ *     then the others by importance, larger first, ties to the lower block; slots
+ *     left over are -1.
+ *
+ * nsa_compress_kv: k, v [N, h_k, d] (dims->dtype) -> kc, vc [R, h_k, d] with
+ *   R = floor(N / kernel_stride) rows allocated by the caller (an upper bound on the
+ *   compressed tokens when kernel_size >= kernel_stride); the compressed tokens of
+ *   sequence s are rows cu_cmp[s] .. cu_cmp[s+1] - 1, and cu_cmp (int32 [S + 1],
+ *   written here) ends at their total.  Means are taken in fp32 and rounded to the
+ *   dtype.  Malformed cu_seqlens set NSA_DEVERR_BAD_SEQLENS in *device_status (may
+ *   be NULL).
+ * nsa_cmp_attn_select: q [N, h_q, d], kc / vc and cu_cmp from nsa_compress_kv ->
+ *   out [N, h_q, d] (dtype), lse float32 [h_q, N], sel_idx int32 [h_k, N, topk]
+ *   (dims->block_size = B_K, dims->topk = T), ready for nsa_sel_attn_fwd.
+ *   max_seqlen bounds every sequence's length: it sizes the shared-memory
+ *   importance rows (NSA_ERR_UNSUPPORTED when they cannot fit); a longer sequence
+ *   sets NSA_DEVERR_BAD_SEQLENS and its tokens are left unwritten.  Importance is
+ *   summed in fp32, so blocks whose importance differs by rounding may be chosen in
+ *   either order.
+ * Both: d in {64, 128}; kernel_size >= kernel_stride >= 1; g <= 128; q, kc, vc, out,
+ * k, v 16-byte aligned; errors are returned before any launch. */
+NSA_API nsa_status nsa_compress_kv(const nsa_sel_attn_dims *dims, const int32_t *cu_seqlens,
+                                   int kernel_size, int kernel_stride, const void *k,
+                                   const void *v, void *kc, void *vc, int32_t *cu_cmp,
+                                   int32_t *device_status, nsa_stream_t stream);
+NSA_API nsa_status nsa_cmp_attn_select(const nsa_sel_attn_dims *dims, const void *q,
+                                       const void *kc, const void *vc,
+                                       const int32_t *cu_seqlens, const int32_t *cu_cmp,
+                                       int kernel_size, int kernel_stride, int max_seqlen,
+                                       float scale, int init_blocks, int local_blocks,
+                                       void *out, float *lse, int32_t *sel_idx,
+                                       int32_t *device_status, nsa_stream_t stream);
+
 NSA_API nsa_status nsa_sel_attn_decode(const nsa_sel_attn_dims *dims, const void *q,
                                        const void *k_cache, const void *v_cache,
                                        const int32_t *sel_idx, const int32_t *cu_seqlens,

@@ -131,13 +131,11 @@ def block_importance(probs_t, tau: int, h_k: int, block: int, kernel_size: int, 
     g = h_q // h_k
     nb = tau // block + 1
     imp = np.zeros((h_k, nb))
-    for j in range(nb):
-        lo, hi = j * block, j * block + block            # the block's keys [lo, hi)
-        for i in range(nv):
-            a, b = i * stride, i * stride + kernel_size  # the window's keys [a, b)
-            if a < hi and lo < b:
-                for h in range(h_k):
-                    imp[h, j] += probs_t[h * g:(h + 1) * g, i].sum()
+    for i in range(nv):
+        a, b = i * stride, i * stride + kernel_size      # the window's keys [a, b)
+        w = probs_t[:, i].reshape(h_k, g).sum(axis=1)    # summed over each group's heads
+        for j in range(a // block, (b - 1) // block + 1):  # the blocks holding those keys
+            imp[:, j] += w
     return imp
 
 

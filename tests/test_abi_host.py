@@ -97,6 +97,32 @@ def test_validation_returns_before_launch(lib):
     assert st == 2
 
 
+def test_compressed_branch_validation_returns_before_launch(lib):
+    # nsa_compress_kv / nsa_cmp_attn_select reject bad arguments before any launch
+    d = _dims()
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    st = lib.nsa_compress_kv(ctypes.byref(d), fake, 16, 32, fake, fake, fake, fake, fake, None,
+                             None)
+    assert st == 1                       # kernel_size < kernel_stride
+    st = lib.nsa_compress_kv(ctypes.byref(d), fake, 32, 16, odd, fake, fake, fake, fake, None,
+                             None)
+    assert st == 1                       # k not 16-byte aligned
+    st = lib.nsa_compress_kv(ctypes.byref(_dims(head_dim=256)), fake, 32, 16, fake, fake, fake,
+                             fake, fake, None, None)
+    assert st == 2                       # d = 256 not offered
+    args = (fake, fake, fake, fake, fake, 32, 16)
+    st = lib.nsa_cmp_attn_select(ctypes.byref(d), *args, 0, 0.1, 1, 2, fake, fake, fake, None,
+                                 None)
+    assert st == 1                       # max_seqlen < 1
+    st = lib.nsa_cmp_attn_select(ctypes.byref(d), *args, 8192, 0.1, -1, 2, fake, fake, fake,
+                                 None, None)
+    assert st == 1                       # negative init_blocks
+    st = lib.nsa_cmp_attn_select(ctypes.byref(d), *args, 1 << 30, 0.1, 1, 2, fake, fake, fake,
+                                 None, None)
+    assert st == 2                       # importance rows cannot fit in shared memory
+
+
 def test_status_strings_and_kernel_names(lib):
     import block_sparse_attention_nsa_gb300 as nsa
     for code in range(7):
