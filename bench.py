@@ -33,9 +33,9 @@ DOMINANT = ("fwd_main", "bwd_main")
 # kernels on the 64K workload, from one ncu capture of the kernel sources whose
 # SHA-256 is given (profiles/dram_traffic_fwd64k_g4.md).  Reported only while the
 # sources are unchanged; otherwise the roofline's traffic is null.
-TRAFFIC = {"sources_sha256": "c5478fdc15b4a1d498d022992736a416f7341be0c3cad5fd82635c892dd966c5",
-           "bytes": {"fwd_main": {"4": 925593088 + 4402661632},
-                     "bwd_main": {"4": 2847239680 + 4798372864}}}
+TRAFFIC = {"sources_sha256": "af575b1f509e5d2968713318f8cec0af0db4dfdba57a922d102f3d09f0504845",
+           "bytes": {"fwd_main": {"4": 925123584 + 4402550272},
+                     "bwd_main": {"4": 2803296768 + 4799177216}}}
 
 
 def kernel_sources_hash() -> str:

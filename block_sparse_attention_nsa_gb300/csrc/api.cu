@@ -6,6 +6,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "compress.cuh"
 
 namespace nsa {
 cudaError_t launch_index(const Params &p, cudaStream_t s, void (*mark)(int, cudaStream_t, bool));

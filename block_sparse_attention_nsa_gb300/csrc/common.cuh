@@ -106,21 +106,6 @@ inline Fn driver_entry(const char *name) {
   return reinterpret_cast<Fn>(fn);
 }
 
-// Compressed branch and block selection (compress.cu).
-struct CmpParams {
-  const void *q, *kc, *vc;
-  const int32_t *cu, *cu_cmp;
-  int num_seqs, n, h_q, h_k, g;
-  int ksize, stride, block, topk, init_blocks, local_blocks;
-  int max_seqlen, tt, nb_max;
-  int64_t rows_cap;   // rows allocated for kc / vc
-  float scale_log2;
-  void *out;
-  float *lse;
-  int32_t *sel;
-  int32_t *status;
-};
-
 // ---------------------------------------------------------------------------
 // Small device helpers
 // ---------------------------------------------------------------------------

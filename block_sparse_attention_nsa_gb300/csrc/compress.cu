@@ -20,7 +20,7 @@
 // compressed keys (out, lse); pass 2 recomputes the scores, forms the exact
 // probabilities from lse and adds them into a shared-memory importance row per
 // token; a warp per token then takes the top T.
-#include "common.cuh"
+#include "compress.cuh"
 
 namespace nsa {
 

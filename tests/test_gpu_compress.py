@@ -4,7 +4,8 @@ The step that produces sel_idx: compression (kernel_size 32, kernel_stride 16),
 attention over the compressed tokens, block importance and top-T selection with the
 init and local blocks forced (Flash-Sparse-Attention README, "Usage").  Compressed
 rows and offsets are compared element by element; out and lse to the forward's
-tolerances; the selection, whose ranking is decided by fp32 sums on the GPU and fp64
+tolerances, with the oracle's compressed tokens rounded once to the 16-bit type the
+path stores them in; the selection, whose ranking is decided by fp32 sums on the GPU and fp64
 sums in the oracle, is compared where the oracle's ranking is unique and checked
 for validity where blocks tie within rounding."""
 import numpy as np
@@ -45,9 +46,21 @@ def test_compress_kv_matches_oracle(d, dtype):
     rk, rv = oc.compress_kv(inp["cu_seqlens"], _f64(inp["k"]), _f64(inp["v"]), L_K, STRIDE)
     nc = int(ref_cc[-1])
     assert kc.shape[0] == cfg.n // STRIDE >= nc
-    # fp32 sums of 16-bit inputs, one rounding to 16 bits
-    np.testing.assert_allclose(_f64(kc[:nc]), rk, rtol=8e-3, atol=1e-3)
-    np.testing.assert_allclose(_f64(vc[:nc]), rv, rtol=8e-3, atol=1e-3)
+    # fp32 sums of 16-bit inputs, one rounding to 16 bits: within one unit in the last
+    # place of the exact mean rounded to that type
+    u = 2.0 ** -7 if dtype == "bf16" else 2.0 ** -10
+    for got, ref in ((kc[:nc], rk), (vc[:nc], rv)):
+        r16 = _round16(ref, dtype)
+        ulp = u * 2.0 ** np.floor(np.log2(np.maximum(np.abs(r16), 1e-30)))
+        ulp = np.maximum(ulp, 2.0 ** -24 if dtype == "fp16" else 0.0)   # fp16 subnormals
+        assert (np.abs(_f64(got) - r16) <= ulp + 1e-30).all()
+
+
+def _round16(x, dtype):
+    """The oracle's exact compressed tokens rounded once to the 16-bit type the path
+    stores them in (the header's contract for nsa_compress_kv)."""
+    t = {"bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
+    return torch.from_numpy(x).to(t).double().numpy()
 
 
 def _check_selection(sel, ref_sel, imps, taus, block, topk, init, local, what):
@@ -93,6 +106,7 @@ def test_cmp_attn_select_matches_oracle(g, d, dtype):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     rk, rv = oc.compress_kv(inp["cu_seqlens"], _f64(inp["k"]), _f64(inp["v"]), L_K, STRIDE)
+    rk, rv = _round16(rk, dtype), _round16(rv, dtype)
     toks = list(range(cfg.n))
     ref_sel, imps, ref_out, ref_lse = oc.select_rows(inp["cu_seqlens"], _f64(inp["q"]), rk, rv,
                                                      L_K, STRIDE, cfg.scale, block, topk, init,
@@ -122,6 +136,7 @@ def test_cmp_attn_select_64k_sampled():
     rng = np.random.default_rng(3)
     toks = sorted(set(rng.integers(0, 65536, 60).tolist()) | {0, 30, 31, 63, 64, 1023, 65535})
     rk, rv = oc.compress_kv(inp["cu_seqlens"], _f64(inp["k"]), _f64(inp["v"]), L_K, STRIDE)
+    rk, rv = _round16(rk, "bf16"), _round16(rv, "bf16")
     ref_sel, imps, ref_out, ref_lse = oc.select_rows(inp["cu_seqlens"], _f64(inp["q"]), rk, rv,
                                                      L_K, STRIDE, cfg.scale, block, topk, init,
                                                      local, toks)
