@@ -7,7 +7,8 @@ or a call fails, an exception is raised.
 
 Names follow the C ABI in include/nsa_sel_attn.h:
   workspace_size, index, index_view, fwd, bwd, decode, step_host, get_status,
-  profile_enable, profile_collect.
+  window_select, fwd_window, bwd_window, gate_combine, gate_combine_bwd,
+  compress_kv, cmp_attn_select, profile_enable, profile_collect.
 """
 from __future__ import annotations
 

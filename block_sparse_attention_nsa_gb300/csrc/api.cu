@@ -512,6 +512,7 @@ struct StepAux {
   int device = -1;
   cudaStream_t side = nullptr;
   cudaEvent_t dout_in = nullptr, fwd_done = nullptr, out_back = nullptr;
+  cudaEvent_t kv_in = nullptr, q_in = nullptr;
 };
 static bool step_aux(StepAux **aux) {
   static std::mutex mu;
@@ -529,7 +530,9 @@ static bool step_aux(StepAux **aux) {
   if (cudaStreamCreateWithFlags(&a.side, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&a.dout_in, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&a.fwd_done, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&a.out_back, cudaEventDisableTiming) != cudaSuccess)
+      cudaEventCreateWithFlags(&a.out_back, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&a.kv_in, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&a.q_in, cudaEventDisableTiming) != cudaSuccess)
     return false;
   all.reserve(16);
   all.push_back(a);
@@ -571,45 +574,54 @@ nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const void *hos
   StepAux *aux = nullptr;
   if (!step_aux(&aux)) return NSA_ERR_CUDA;
   cudaStream_t s2 = aux->side;
-  // dout travels on the side stream while the forward runs; out and lse travel back
-  // on it while the backward runs
-  if (cudaEventRecord(aux->fwd_done, s) != cudaSuccess ||            // s2 after s's earlier work
-      cudaStreamWaitEvent(s2, aux->fwd_done, 0) != cudaSuccess)
+  // The forward's inputs go first, split over the two streams: k and v on the side
+  // stream, sel, cu_seqlens and q on the caller's.  dout follows on the side stream
+  // once q has landed, so that it shares the host link with the forward's compute
+  // rather than with the forward's inputs.  out and lse travel back on the side stream
+  // while the backward runs; the gradients go back split over the two streams.
+  struct Copy { void *dst; const void *src; size_t n; };
+  auto copies = [](const Copy *c, int nc, cudaMemcpyKind kind, cudaStream_t st_) {
+    for (int i = 0; i < nc; ++i)
+      if (c[i].n && cudaMemcpyAsync(c[i].dst, c[i].src, c[i].n, kind, st_) != cudaSuccess)
+        return false;
+    return true;
+  };
+  auto join = [](cudaEvent_t ev, cudaStream_t from, cudaStream_t to) {   // to waits for from
+    return cudaEventRecord(ev, from) == cudaSuccess &&
+           cudaStreamWaitEvent(to, ev, 0) == cudaSuccess;
+  };
+  const Copy in_kv[] = {{k, host_k, kbytes}, {v, host_v, kbytes}};
+  const Copy in_q[] = {{sel, host_sel_idx, selbytes}, {cu, host_cu_seqlens, cubytes},
+                       {q, host_q, qbytes}};
+  const Copy in_do[] = {{dout, host_dout, qbytes}};
+  if (!join(aux->fwd_done, s, s2) ||                       // s2 after s's earlier work
+      !copies(in_kv, 2, cudaMemcpyHostToDevice, s2) ||
+      cudaEventRecord(aux->kv_in, s2) != cudaSuccess ||
+      !copies(in_q, 3, cudaMemcpyHostToDevice, s) || !join(aux->q_in, s, s2) ||
+      !copies(in_do, 1, cudaMemcpyHostToDevice, s2) ||
+      cudaEventRecord(aux->dout_in, s2) != cudaSuccess ||
+      cudaStreamWaitEvent(s, aux->kv_in, 0) != cudaSuccess)
     return NSA_ERR_CUDA;
-  if (qbytes && cudaMemcpyAsync(dout, host_dout, qbytes, cudaMemcpyHostToDevice, s2) != cudaSuccess)
-    return NSA_ERR_CUDA;
-  if (cudaEventRecord(aux->dout_in, s2) != cudaSuccess) return NSA_ERR_CUDA;
-  const struct { void *dst; const void *src; size_t n; } h2d[] = {
-      {sel, host_sel_idx, selbytes}, {cu, host_cu_seqlens, cubytes}, {q, host_q, qbytes},
-      {k, host_k, kbytes}, {v, host_v, kbytes}};
-  for (const auto &c : h2d)
-    if (c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return NSA_ERR_CUDA;
   st = nsa_sel_attn_fwd(dims, q, k, v, reinterpret_cast<int32_t *>(sel),
                         reinterpret_cast<int32_t *>(cu), scale, out, reinterpret_cast<float *>(lse),
                         workspace, workspace_bytes, stream);
   if (st != NSA_OK) return st;
-  if (cudaEventRecord(aux->fwd_done, s) != cudaSuccess ||
-      cudaStreamWaitEvent(s2, aux->fwd_done, 0) != cudaSuccess)
-    return NSA_ERR_CUDA;
-  const struct { void *dst; const void *src; size_t n; } back1[] = {
-      {host_out, out, qbytes}, {host_lse, lse, host_lse ? lsebytes : 0}};
-  for (const auto &c : back1)
-    if (c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToHost, s2) != cudaSuccess)
-      return NSA_ERR_CUDA;
-  if (cudaEventRecord(aux->out_back, s2) != cudaSuccess ||
+  const Copy back1[] = {{host_out, out, qbytes}, {host_lse, lse, host_lse ? lsebytes : 0}};
+  if (!join(aux->fwd_done, s, s2) || !copies(back1, 2, cudaMemcpyDeviceToHost, s2) ||
+      cudaEventRecord(aux->out_back, s2) != cudaSuccess ||
       cudaStreamWaitEvent(s, aux->dout_in, 0) != cudaSuccess)
     return NSA_ERR_CUDA;
   st = nsa_sel_attn_bwd(dims, q, k, v, reinterpret_cast<int32_t *>(sel),
                         reinterpret_cast<int32_t *>(cu), scale, out, reinterpret_cast<float *>(lse),
                         dout, dq, dk, dv, workspace, workspace_bytes, 1, stream);
   if (st != NSA_OK) return st;
-  const struct { void *dst; const void *src; size_t n; } back2[] = {
-      {host_dq, dq, qbytes}, {host_dk, dk, kbytes}, {host_dv, dv, kbytes}};
-  for (const auto &c : back2)
-    if (c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-      return NSA_ERR_CUDA;
-  if (cudaStreamWaitEvent(s, aux->out_back, 0) != cudaSuccess) return NSA_ERR_CUDA;
+  const Copy back_kv[] = {{host_dk, dk, kbytes}, {host_dv, dv, kbytes}};
+  const Copy back_q[] = {{host_dq, dq, qbytes}};
+  if (!join(aux->fwd_done, s, s2) || !copies(back_kv, 2, cudaMemcpyDeviceToHost, s2) ||
+      cudaEventRecord(aux->kv_in, s2) != cudaSuccess ||
+      !copies(back_q, 1, cudaMemcpyDeviceToHost, s) ||
+      cudaStreamWaitEvent(s, aux->kv_in, 0) != cudaSuccess)   // after out, lse, dk and dv
+    return NSA_ERR_CUDA;
   return cuda_status(cudaStreamSynchronize(s));
 }
 

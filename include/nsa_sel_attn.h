@@ -139,10 +139,10 @@ NSA_API nsa_status nsa_sel_attn_staging_size(const nsa_sel_attn_dims *dims, size
 /* One training step of the branch from HOST buffers: copies q, k, v, dout,
  * sel_idx and cu_seqlens to the caller's device staging buffer, runs forward and
  * backward (reusing the index), copies out, lse, dq, dk and dv back to the host
- * buffers, and synchronises the stream.  dout is uploaded, and out and lse are
- * downloaded, on a side stream that the library creates once per device, so those
- * copies overlap the forward and the backward; the call returns only after every
- * copy of both streams is complete.  Host buffers should be pinned for the copies
+ * buffers, and synchronises the stream.  A side stream, created once per device by
+ * the library, carries k and v up beside q, then dout while the forward runs, out and
+ * lse down while the backward runs, and dk and dv down beside dq; the call returns
+ * only after every copy of both streams is complete.  Host buffers should be pinned for the copies
  * to be asynchronous.  host_lse may be NULL to skip that copy. */
 NSA_API nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const void *host_q,
                                   const void *host_k, const void *host_v,
@@ -155,9 +155,9 @@ NSA_API nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const v
 /* Size of the fixed scratch array used by nsa_sel_attn_fwd_noalloc (16 MiB). */
 #define NSA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
-/* Forward without any device allocation, for callers that cannot allocate: code
- * running during CUDA graph capture, plugins whose host framework owns all device
- * memory, loops that cannot afford an allocation's synchronisation.  Same inputs,
+/* Forward without any device allocation, for callers that cannot allocate:
+ * plugins whose host framework owns all device memory, loops that cannot afford
+ * an allocation's synchronisation.  Same inputs,
  * outputs and results as nsa_sel_attn_fwd, but the scratch is a fixed array of
  * NSA_NOALLOC_SCRATCH_BYTES inside the library (held by every GPU that loads the
  * library until exit).  The paper has no counterpart to this entry point.

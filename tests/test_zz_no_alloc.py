@@ -1,8 +1,8 @@
 """The no-allocation forward, nsa_sel_attn_fwd_noalloc, called through the C ABI.
 
-It exists for callers that cannot allocate device memory (graph capture, host
-frameworks that own all device memory, loops that cannot take an allocation's
-synchronisation); its scratch is a fixed array inside the library.  Its output
+It exists for callers that cannot allocate device memory (host frameworks that
+own all device memory, loops that cannot take an allocation's synchronisation);
+its scratch is a fixed array inside the library.  Its output
 must match the regular nsa_sel_attn_fwd (given a caller-allocated workspace)
 within the forward tolerance, on consecutive calls that reuse the same array.
 This file is named to be collected last.
