@@ -33,9 +33,9 @@ DOMINANT = ("fwd_main", "bwd_main")
 # kernels on the 64K workload, from one ncu capture of the kernel sources whose
 # SHA-256 is given (profiles/dram_traffic_fwd64k_g4.md).  Reported only while the
 # sources are unchanged; otherwise the roofline's traffic is null.
-TRAFFIC = {"sources_sha256": "af575b1f509e5d2968713318f8cec0af0db4dfdba57a922d102f3d09f0504845",
-           "bytes": {"fwd_main": {"4": 925123584 + 4402550272},
-                     "bwd_main": {"4": 2803296768 + 4799177216}}}
+TRAFFIC = {"sources_sha256": "85346f7ef6ca29893f13861d7768a170b58438dee8d6b9be5fc95d35b118f397",
+           "bytes": {"fwd_main": {"4": 926530560 + 4402446080},
+                     "bwd_main": {"4": 2839857408 + 4798196224}}}
 
 
 def kernel_sources_hash() -> str:

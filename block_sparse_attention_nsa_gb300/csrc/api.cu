@@ -63,7 +63,14 @@ struct Profiler {
   }
 } g_prof;
 
+// Set by the host-buffer step around its backward: recorded once dk and dv are
+// final (the end of the dK/dV reduction, kernel id 10).
+thread_local cudaEvent_t t_dkv_ready = nullptr;
+thread_local bool t_dkv_recorded = false;
+
 void mark(int id, cudaStream_t stream, bool begin) {
+  if (id == 10 && !begin && t_dkv_ready)
+    t_dkv_recorded = cudaEventRecord(t_dkv_ready, stream) == cudaSuccess;
   if (!g_prof.on) return;
   cudaEvent_t e = g_prof.get();
   if (!e) return;
@@ -611,13 +618,20 @@ nsa_status nsa_sel_attn_step_host(const nsa_sel_attn_dims *dims, const void *hos
       cudaEventRecord(aux->out_back, s2) != cudaSuccess ||
       cudaStreamWaitEvent(s, aux->dout_in, 0) != cudaSuccess)
     return NSA_ERR_CUDA;
+  t_dkv_ready = aux->kv_in;
+  t_dkv_recorded = false;
   st = nsa_sel_attn_bwd(dims, q, k, v, reinterpret_cast<int32_t *>(sel),
                         reinterpret_cast<int32_t *>(cu), scale, out, reinterpret_cast<float *>(lse),
                         dout, dq, dk, dv, workspace, workspace_bytes, 1, stream);
+  t_dkv_ready = nullptr;
   if (st != NSA_OK) return st;
+  // dk and dv go down on the side stream once their reduction is done, while the dQ
+  // reduction still runs; without that record, after the whole backward
+  if (!t_dkv_recorded && cudaEventRecord(aux->kv_in, s) != cudaSuccess) return NSA_ERR_CUDA;
   const Copy back_kv[] = {{host_dk, dk, kbytes}, {host_dv, dv, kbytes}};
   const Copy back_q[] = {{host_dq, dq, qbytes}};
-  if (!join(aux->fwd_done, s, s2) || !copies(back_kv, 2, cudaMemcpyDeviceToHost, s2) ||
+  if (cudaStreamWaitEvent(s2, aux->kv_in, 0) != cudaSuccess ||
+      !copies(back_kv, 2, cudaMemcpyDeviceToHost, s2) ||
       cudaEventRecord(aux->kv_in, s2) != cudaSuccess ||
       !copies(back_q, 1, cudaMemcpyDeviceToHost, s) ||
       cudaStreamWaitEvent(s, aux->kv_in, 0) != cudaSuccess)   // after out, lse, dk and dv

@@ -770,14 +770,17 @@ static cudaError_t run_bwd(const Params &p, int num_sms, int64_t max_tiles, cuda
   mark(8, stream, true);
   kern<<<static_cast<unsigned>(grid), L::kThreads, smem, stream>>>(mk, mv, mdq, p);
   mark(8, stream, false);
-  mark(9, stream, true);
-  bwd_dq_kernel<D, kFp16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
-  mark(9, stream, false);
+  // dK/dV first: the two reductions are independent, and dk/dv are then final while
+  // the larger dQ reduction runs (the end of mark 10 is where a caller may start
+  // copying them)
   mark(10, stream, true);
   bwd_dkv_kernel<D, BK, kFp16>
       <<<dim3(static_cast<unsigned>(p.h_k * p.nb_max), BK / kDkvKeys), kDkvKeys * D / 4, 0,
          stream>>>(p);
   mark(10, stream, false);
+  mark(9, stream, true);
+  bwd_dq_kernel<D, kFp16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+  mark(9, stream, false);
   return cudaGetLastError();
 }
 

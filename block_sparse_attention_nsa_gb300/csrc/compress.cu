@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(256) cmp_attn_select_kernel(const CmpParams p)
   const uint16_t *kc = static_cast<const uint16_t *>(p.kc);
   const uint16_t *vc = static_cast<const uint16_t *>(p.vc);
   const uint64_t keep = l2_evict_last();
+  const bool quad = p.block == 4 * p.stride && p.ksize == 2 * p.stride;
 
   const int s_first = seq_of(p.cu, p.num_seqs, t0);
   const int s_last = seq_of(p.cu, p.num_seqs, t_end - 1);
@@ -376,14 +377,29 @@ __global__ void __launch_bounds__(256) cmp_attn_select_kernel(const CmpParams p)
       const int nj = j1 - j0 + 1;
       for (int w = tid; w < ntok * nj; w += blockDim.x) {
         const int tl = tl0 + w / nj, j = j0 + w % nj;
-        // windows overlapping keys [j*B, j*B + B): i*stride < j*B + B, i*stride + l > j*B
-        const int lo_num = j * p.block - p.ksize + 1;
-        const int ilo = max(i0, lo_num > 0 ? (lo_num + p.stride - 1) / p.stride : 0);
-        const int ihi = min(i1, (j * p.block + p.block - 1) / p.stride);
         float acc = 0.f;
-        for (int h = 0; h < p.g; ++h) {
-          const float *prow = ps + (tl * p.g + h) * kPsStride - i0;
-          for (int i = ilo; i <= ihi; ++i) acc += prow[i];
+        if (quad) {
+          // B = 4 stride, l = 2 stride: block j - j0 is overlapped by the chunk's
+          // windows 4 (j - j0) - 1 .. 4 (j - j0) + 3 (columns past the visible ones
+          // hold 0); the first of them belongs to the previous chunk when j = j0
+          const int jr = j - j0;
+          for (int h = 0; h < p.g; ++h) {
+            const float *prow = ps + (tl * p.g + h) * kPsStride;
+            if (jr < kCmpChunk / 4) {
+              const float4 x = *reinterpret_cast<const float4 *>(prow + 4 * jr);
+              acc += (x.x + x.y) + (x.z + x.w);
+            }
+            if (jr >= 1) acc += prow[4 * jr - 1];
+          }
+        } else {
+          // windows overlapping keys [j*B, j*B + B): i*stride < j*B + B, i*stride + l > j*B
+          const int lo_num = j * p.block - p.ksize + 1;
+          const int ilo = max(i0, lo_num > 0 ? (lo_num + p.stride - 1) / p.stride : 0);
+          const int ihi = min(i1, (j * p.block + p.block - 1) / p.stride);
+          for (int h = 0; h < p.g; ++h) {
+            const float *prow = ps + (tl * p.g + h) * kPsStride - i0;
+            for (int i = ilo; i <= ihi; ++i) acc += prow[i];
+          }
         }
         imp[tl * p.nb_max + j] += acc;
       }

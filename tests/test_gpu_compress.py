@@ -90,12 +90,15 @@ def _check_selection(sel, ref_sel, imps, taus, block, topk, init, local, what):
     return exact
 
 
-@pytest.mark.parametrize("g,d,dtype", [(1, 128, "bf16"), (4, 128, "bf16"), (3, 64, "fp16"),
-                                       (16, 128, "bf16"), (2, 64, "bf16")])
-def test_cmp_attn_select_matches_oracle(g, d, dtype):
-    # ragged sequences: empty, shorter than one window, a partial chunk, several chunks
+@pytest.mark.parametrize("g,d,dtype,block", [(1, 128, "bf16", 64), (4, 128, "bf16", 64),
+                                             (3, 64, "fp16", 64), (16, 128, "bf16", 64),
+                                             (2, 64, "bf16", 32), (1, 64, "fp16", 128)])
+def test_cmp_attn_select_matches_oracle(g, d, dtype, block):
+    # ragged sequences: empty, shorter than one window, a partial chunk, several chunks;
+    # B_K = 64 = 4 strides takes the kernel's aligned importance path, 32 and 128 the
+    # general one
     seqlens = [700, 0, 20, 31, 33, 2100, 130]
-    block, topk, init, local = 64, 6, 1, 2
+    topk, init, local = 6, 1, 2
     cfg, inp, dev = _inputs(seqlens, 2, g, d, dtype, 17 + g)
     import block_sparse_attention_nsa_gb300 as nsa
     kc, vc, cu_cmp = nsa.compress_kv(dev["k"], dev["v"], dev["cu"], L_K, STRIDE)
