@@ -33,9 +33,9 @@ DOMINANT = ("fwd_main", "bwd_main")
 # kernels on the 64K workload, from one ncu capture of the kernel sources whose
 # SHA-256 is given (profiles/dram_traffic_fwd64k_g4.md).  Reported only while the
 # sources are unchanged; otherwise the roofline's traffic is null.
-TRAFFIC = {"sources_sha256": "85346f7ef6ca29893f13861d7768a170b58438dee8d6b9be5fc95d35b118f397",
-           "bytes": {"fwd_main": {"4": 926530560 + 4402446080},
-                     "bwd_main": {"4": 2839857408 + 4798196224}}}
+TRAFFIC = {"sources_sha256": "87a067ecf4360de5264f173ed906895dcefa0d9414666f4f7cabb0b219484bd9",
+           "bytes": {"fwd_main": {"4": 927921408 + 4402221056},
+                     "bwd_main": {"4": 2872249856 + 4798644224}}}
 
 
 def kernel_sources_hash() -> str:
@@ -496,9 +496,14 @@ def cmp_sweep(torch, dev, pk_burst):
         def comp():
             state["c"] = nsa.compress_kv(k, v, cu, 32, 16)
 
+        dims = nsa.make_dims(1, c.n, c.h_q, c.h_k, c.d, 64, 16, q.dtype)
+        need = nsa.cmp_workspace_size(dims, 32, 16, c.n)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+
         def sel():
             kc, vc, cc = state["c"]
-            nsa.cmp_attn_select(q, kc, vc, cu, cc, 32, 16, c.n, c.scale, 64, 16, 1, 2)
+            nsa.cmp_attn_select(q, kc, vc, cu, cc, 32, 16, c.n, c.scale, 64, 16, 1, 2,
+                                workspace=ws)
         comp()
         sel()
         torch.cuda.synchronize()
@@ -512,7 +517,7 @@ def cmp_sweep(torch, dev, pk_burst):
             "useful_tflops": ff / (s_ms * 1e-3) / 1e12,
             "issued_tflops": 1.5 * ff / (s_ms * 1e-3) / 1e12,
             "pct_peak_issued": 100 * 1.5 * ff / (s_ms * 1e-3) / 1e12 / pk_burst}
-        del q, k, v, state
+        del q, k, v, state, ws
         torch.cuda.empty_cache()
     return outd
 

@@ -20,7 +20,7 @@ import torch
 
 __all__ = ["Dims", "NsaError", "load", "workspace_size", "index", "index_view", "fwd", "bwd",
            "decode", "window_select", "fwd_window", "bwd_window", "gate_combine",
-           "gate_combine_bwd", "compress_kv", "cmp_attn_select",
+           "gate_combine_bwd", "compress_kv", "cmp_attn_select", "cmp_workspace_size",
            "staging_size", "step_host", "get_status", "profile_enable", "profile_collect",
            "kernel_names", "make_dims", "LIB_PATH"]
 
@@ -86,7 +86,9 @@ def load():
                                  vp]),
         "nsa_cmp_attn_select": (st, [dp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, f32, ctypes.c_int, ctypes.c_int, vp, vp, vp,
-                                     vp, vp]),
+                                     vp, vp, sz, vp]),
+        "nsa_cmp_workspace_size": (st, [dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.POINTER(sz)]),
         "nsa_sel_attn_num_kernels": (i32, []),
         "nsa_sel_attn_kernel_name": (ctypes.c_char_p, [i32]),
         "nsa_sel_attn_profile_enable": (st, [i32]),
@@ -275,16 +277,36 @@ def compress_kv(k, v, cu_seqlens, kernel_size: int, kernel_stride: int, device_s
     return kc, vc, cu_cmp
 
 
+def cmp_workspace_size(dims: Dims, kernel_size: int, kernel_stride: int,
+                       max_seqlen: int) -> int:
+    """Workspace bytes of cmp_attn_select (0 when shared memory holds the rows)."""
+    b = ctypes.c_size_t()
+    _check(load().nsa_cmp_workspace_size(ctypes.byref(dims), int(kernel_size),
+                                         int(kernel_stride), int(max_seqlen), ctypes.byref(b)),
+           "cmp_workspace_size")
+    return b.value
+
+
 def cmp_attn_select(q, kc, vc, cu_seqlens, cu_cmp, kernel_size: int, kernel_stride: int,
                     max_seqlen: int, scale: float, block_size: int, topk: int,
                     init_blocks: int = 1, local_blocks: int = 2, device_status=None,
+                    workspace: Optional[torch.Tensor] = None, use_workspace: bool = True,
                     stream=None):
     """Compressed attention and top-T block selection: out [N, h_q, d], lse float32
-    [h_q, N] and sel_idx int32 [h_k, N, topk]."""
+    [h_q, N] and sel_idx int32 [h_k, N, topk].  workspace: uint8 device tensor of at
+    least cmp_workspace_size bytes; allocated here when None and needed, and never
+    passed when use_workspace is False (the importance rows then stay in shared
+    memory, in smaller CTAs)."""
     _contig(q, kc, vc, cu_seqlens, cu_cmp)
     n, h_q, d = q.shape
     h_k = kc.shape[1]
     dims = make_dims(cu_seqlens.numel() - 1, n, h_q, h_k, d, block_size, topk, q.dtype)
+    if not use_workspace:
+        workspace = None
+    elif workspace is None:
+        need = cmp_workspace_size(dims, kernel_size, kernel_stride, max_seqlen)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     out = torch.empty_like(q)
     lse = torch.empty((h_q, n), dtype=torch.float32, device=q.device)
     sel = torch.empty((h_k, n, topk), dtype=torch.int32, device=q.device)
@@ -292,6 +314,7 @@ def cmp_attn_select(q, kc, vc, cu_seqlens, cu_cmp, kernel_size: int, kernel_stri
         ctypes.byref(dims), _ptr(q), _ptr(kc), _ptr(vc), _ptr(cu_seqlens), _ptr(cu_cmp),
         int(kernel_size), int(kernel_stride), int(max_seqlen), float(scale), int(init_blocks),
         int(local_blocks), _ptr(out), _ptr(lse), _ptr(sel), _ptr(device_status),
+        _ptr(workspace), 0 if workspace is None else workspace.numel(),
         _stream(stream)), "cmp_attn_select")
     return out, lse, sel
 

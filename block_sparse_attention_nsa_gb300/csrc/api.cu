@@ -32,7 +32,7 @@ cudaError_t launch_compress(int d, bool fp16, const int32_t *cu, const int32_t *
                             int64_t rows_cap, const void *k, const void *v, void *kc, void *vc,
                             cudaStream_t s);
 cudaError_t launch_cmp_select(int d, bool fp16, const CmpParams &p, cudaStream_t s);
-int cmp_tokens_per_cta(int d, int g, int nb_max);
+int cmp_tokens_per_cta(int d, int g, int nb_max, bool in_smem);
 
 namespace {
 
@@ -689,11 +689,43 @@ nsa_status nsa_compress_kv(const nsa_sel_attn_dims *dims, const int32_t *cu_seql
                                      kernel_stride, rows_cap, k, v, kc, vc, s));
 }
 
+// Launch shape of nsa_cmp_attn_select: tokens per CTA and the workspace bytes that
+// the importance rows take in global memory (0 when shared memory holds them in a
+// CTA of full size, or when no workspace is offered).
+static nsa_status cmp_plan(const nsa_sel_attn_dims *dims, int max_seqlen, bool ws_ok, int *tt,
+                           int *nb_max, size_t *ws_bytes) {
+  const int g = dims->h_q / dims->h_k;
+  const int64_t nb = ((int64_t)max_seqlen + dims->block_size - 1) / dims->block_size;
+  if (nb > (int64_t(1) << 20)) return NSA_ERR_UNSUPPORTED;
+  *nb_max = static_cast<int>(nb);
+  const int tt_smem = cmp_tokens_per_cta(dims->head_dim, g, *nb_max, true);
+  const int tt_full = cmp_tokens_per_cta(dims->head_dim, g, *nb_max, false);
+  *ws_bytes = 0;
+  if (tt_smem == tt_full || !ws_ok) {
+    *tt = tt_smem;
+    return tt_smem ? NSA_OK : NSA_ERR_UNSUPPORTED;
+  }
+  *tt = tt_full;
+  const int64_t ctas = ((int64_t)dims->total_tokens + tt_full - 1) / tt_full * dims->h_k;
+  *ws_bytes = static_cast<size_t>(ctas) * tt_full * (*nb_max) * sizeof(float);
+  return NSA_OK;
+}
+
+nsa_status nsa_cmp_workspace_size(const nsa_sel_attn_dims *dims, int kernel_size,
+                                  int kernel_stride, int max_seqlen, size_t *bytes) {
+  nsa_status st = check_cmp(dims, kernel_size, kernel_stride);
+  if (st != NSA_OK) return st;
+  if (max_seqlen < 1 || !bytes) return NSA_ERR_INVALID_ARG;
+  int tt = 0, nb = 0;
+  return cmp_plan(dims, max_seqlen, true, &tt, &nb, bytes);
+}
+
 nsa_status nsa_cmp_attn_select(const nsa_sel_attn_dims *dims, const void *q, const void *kc,
                                const void *vc, const int32_t *cu_seqlens, const int32_t *cu_cmp,
                                int kernel_size, int kernel_stride, int max_seqlen, float scale,
                                int init_blocks, int local_blocks, void *out, float *lse,
-                               int32_t *sel_idx, int32_t *device_status, nsa_stream_t stream) {
+                               int32_t *sel_idx, int32_t *device_status, void *workspace,
+                               size_t workspace_bytes, nsa_stream_t stream) {
   nsa_status st = check_cmp(dims, kernel_size, kernel_stride);
   if (st != NSA_OK) return st;
   if (max_seqlen < 1 || init_blocks < 0 || local_blocks < 0 || !(scale > 0.f))
@@ -706,10 +738,12 @@ nsa_status nsa_cmp_attn_select(const nsa_sel_attn_dims *dims, const void *q, con
       !aligned(lse, 4) || !aligned(sel_idx, 4) || (device_status && !aligned(device_status, 4)))
     return NSA_ERR_INVALID_ARG;
   const int g = dims->h_q / dims->h_k;
-  const int64_t nb_max = ((int64_t)max_seqlen + dims->block_size - 1) / dims->block_size;
-  if (nb_max > (int64_t(1) << 20)) return NSA_ERR_UNSUPPORTED;
-  const int tt = cmp_tokens_per_cta(dims->head_dim, g, static_cast<int>(nb_max));
-  if (tt == 0) return NSA_ERR_UNSUPPORTED;
+  if (workspace && !aligned(workspace, 16)) return NSA_ERR_INVALID_ARG;
+  int tt = 0, nb_max = 0;
+  size_t ws_need = 0;
+  st = cmp_plan(dims, max_seqlen, workspace != nullptr, &tt, &nb_max, &ws_need);
+  if (st != NSA_OK) return st;
+  if (ws_need > workspace_bytes) return NSA_ERR_WORKSPACE;
   CmpParams p;
   std::memset(&p, 0, sizeof(p));
   p.q = q;
@@ -730,8 +764,9 @@ nsa_status nsa_cmp_attn_select(const nsa_sel_attn_dims *dims, const void *q, con
   p.local_blocks = local_blocks;
   p.max_seqlen = max_seqlen;
   p.tt = tt;
-  p.nb_max = static_cast<int>(nb_max);
+  p.nb_max = nb_max;
   p.rows_cap = rows_cap;
+  p.imp_ws = ws_need ? static_cast<float *>(workspace) : nullptr;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.out = out;
   p.lse = lse;

@@ -156,7 +156,11 @@ __global__ void __launch_bounds__(256) cmp_attn_select_kernel(const CmpParams p)
   constexpr int KS = D / 16;        // k-steps of the score MMA
   constexpr int NT = kCmpChunk / 8; // score n-tiles per chunk
   extern __shared__ __align__(128) uint8_t smem[];
-  float *imp = reinterpret_cast<float *>(smem + L::kImp);
+  // importance rows: this CTA's slice of the caller's workspace when given, else
+  // shared memory
+  float *imp = p.imp_ws ? p.imp_ws + ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) *
+                                         p.tt * p.nb_max
+                        : reinterpret_cast<float *>(smem + L::kImp);
   float *ps = reinterpret_cast<float *>(smem + L::kV);
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -472,12 +476,14 @@ cudaError_t launch_compress(int d, bool fp16, const int32_t *cu, const int32_t *
   }
 }
 
-// Tokens per CTA: the largest power of two <= 64 with at most 128 rows (8 warps) and
-// the importance rows within shared memory; 0 when none fits.
-int cmp_tokens_per_cta(int d, int g, int nb_max) {
+// Tokens per CTA: the largest power of two <= 128 with at most 128 rows (8 warps) and,
+// when the importance rows live in shared memory (in_smem), those rows within it;
+// 0 when none fits.
+int cmp_tokens_per_cta(int d, int g, int nb_max, bool in_smem) {
   const size_t limit = 227 * 1024;
-  for (int tt = 64; tt >= 1; tt >>= 1) {
+  for (int tt = 128; tt >= 1; tt >>= 1) {
     if (tt * g > 128) continue;
+    if (!in_smem) return tt;
     const size_t bytes = d == 64 ? CmpSmem<64>::bytes(tt, nb_max) : CmpSmem<128>::bytes(tt, nb_max);
     if (bytes <= limit) return tt;
   }
@@ -486,7 +492,7 @@ int cmp_tokens_per_cta(int d, int g, int nb_max) {
 
 template <int D, bool kFp16>
 static cudaError_t run_cmp_select(const CmpParams &p, cudaStream_t s) {
-  const size_t smem = CmpSmem<D>::bytes(p.tt, p.nb_max);
+  const size_t smem = p.imp_ws ? CmpSmem<D>::kImp : CmpSmem<D>::bytes(p.tt, p.nb_max);
   auto kern = cmp_attn_select_kernel<D, kFp16>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -12,6 +12,7 @@ struct CmpParams {
   int ksize, stride, block, topk, init_blocks, local_blocks;
   int max_seqlen, tt, nb_max;
   int64_t rows_cap;   // rows allocated for kc / vc
+  float *imp_ws;      // importance rows in global memory (tt * nb_max per CTA), or null
   float scale_log2;
   void *out;
   float *lse;

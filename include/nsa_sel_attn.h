@@ -289,11 +289,17 @@ NSA_API nsa_status nsa_gate_combine_bwd(const nsa_sel_attn_dims *dims, int n_bra
  * nsa_cmp_attn_select: q [N, h_q, d], kc / vc and cu_cmp from nsa_compress_kv ->
  *   out [N, h_q, d] (dtype), lse float32 [h_q, N], sel_idx int32 [h_k, N, topk]
  *   (dims->block_size = B_K, dims->topk = T), ready for nsa_sel_attn_fwd.
- *   max_seqlen bounds every sequence's length: it sizes the shared-memory
- *   importance rows (NSA_ERR_UNSUPPORTED when they cannot fit); a longer sequence
- *   sets NSA_DEVERR_BAD_SEQLENS and its tokens are left unwritten.  Importance is
- *   summed in fp32, so blocks whose importance differs by rounding may be chosen in
- *   either order.
+ *   max_seqlen bounds every sequence's length: it sizes the importance rows, one
+ *   fp32 per causal block of each token; a longer sequence sets
+ *   NSA_DEVERR_BAD_SEQLENS and its tokens are left unwritten.  The rows live in
+ *   shared memory, or, when they would leave a CTA too few tokens there and a
+ *   workspace is given, in that workspace (caller-owned device memory of at least
+ *   nsa_cmp_workspace_size bytes, 16-byte aligned; NULL and 0 allowed).  Too small a
+ *   workspace is NSA_ERR_WORKSPACE; rows that fit neither way NSA_ERR_UNSUPPORTED.
+ *   Importance is summed in fp32, so blocks whose importance differs by rounding may
+ *   be chosen in either order.
+ * nsa_cmp_workspace_size: the workspace bytes nsa_cmp_attn_select uses for these
+ *   dims and max_seqlen (0 when shared memory suffices); host only.
  * Both: d in {64, 128}; kernel_size >= kernel_stride >= 1; g <= 128; q, kc, vc, out,
  * k, v 16-byte aligned; errors are returned before any launch. */
 NSA_API nsa_status nsa_compress_kv(const nsa_sel_attn_dims *dims, const int32_t *cu_seqlens,
@@ -306,7 +312,10 @@ NSA_API nsa_status nsa_cmp_attn_select(const nsa_sel_attn_dims *dims, const void
                                        int kernel_size, int kernel_stride, int max_seqlen,
                                        float scale, int init_blocks, int local_blocks,
                                        void *out, float *lse, int32_t *sel_idx,
-                                       int32_t *device_status, nsa_stream_t stream);
+                                       int32_t *device_status, void *workspace,
+                                       size_t workspace_bytes, nsa_stream_t stream);
+NSA_API nsa_status nsa_cmp_workspace_size(const nsa_sel_attn_dims *dims, int kernel_size,
+                                          int kernel_stride, int max_seqlen, size_t *bytes);
 
 NSA_API nsa_status nsa_sel_attn_decode(const nsa_sel_attn_dims *dims, const void *q,
                                        const void *k_cache, const void *v_cache,

@@ -113,14 +113,26 @@ def test_compressed_branch_validation_returns_before_launch(lib):
     assert st == 2                       # d = 256 not offered
     args = (fake, fake, fake, fake, fake, 32, 16)
     st = lib.nsa_cmp_attn_select(ctypes.byref(d), *args, 0, 0.1, 1, 2, fake, fake, fake, None,
-                                 None)
+                                 None, 0, None)
     assert st == 1                       # max_seqlen < 1
     st = lib.nsa_cmp_attn_select(ctypes.byref(d), *args, 8192, 0.1, -1, 2, fake, fake, fake,
-                                 None, None)
+                                 None, None, 0, None)
     assert st == 1                       # negative init_blocks
     st = lib.nsa_cmp_attn_select(ctypes.byref(d), *args, 1 << 30, 0.1, 1, 2, fake, fake, fake,
-                                 None, None)
-    assert st == 2                       # importance rows cannot fit in shared memory
+                                 None, None, 0, None)
+    assert st == 2                       # importance rows beyond any supported length
+    # one 64K sequence at g = 1: the rows leave a shared-memory CTA two warps, so a
+    # workspace holding them for 128-token CTAs is asked for, and a short one refused
+    d1 = _dims(h_q=d.h_k)
+    b = ctypes.c_size_t()
+    assert lib.nsa_cmp_workspace_size(ctypes.byref(d1), 32, 16, 65536, ctypes.byref(b)) == 0
+    ctas = -(-d1.total_tokens // 128) * d1.h_k
+    assert b.value == ctas * 128 * 1024 * 4
+    st = lib.nsa_cmp_attn_select(ctypes.byref(d1), *args, 65536, 0.1, 1, 2, fake, fake, fake,
+                                 None, fake, 16, None)
+    assert st == 3                       # workspace too small
+    assert lib.nsa_cmp_workspace_size(ctypes.byref(d1), 32, 16, 4096, ctypes.byref(b)) == 0
+    assert b.value == 0                  # short sequences: shared memory suffices
 
 
 def test_status_strings_and_kernel_names(lib):

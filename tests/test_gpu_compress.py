@@ -163,3 +163,38 @@ def test_cmp_attn_select_rejects_long_sequence():
                         device_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) & 2        # NSA_DEVERR_BAD_SEQLENS
+
+
+def test_cmp_attn_select_workspace_rows_match_shared_rows():
+    # g = 1 with a 40K-token sequence: in shared memory the importance rows leave a CTA
+    # 64 tokens, so the call takes 128-token CTAs with the rows in its workspace.  The
+    # per-row arithmetic is the same either way, so both launches agree bit for bit;
+    # sampled rows are also checked against the oracle.
+    seqlens = [40000, 300, 5000]
+    block, topk, init, local = 64, 16, 1, 2
+    cfg, inp, dev = _inputs(seqlens, 2, 1, 64, "bf16", 41)
+    import block_sparse_attention_nsa_gb300 as nsa
+    dims = nsa.make_dims(len(seqlens), cfg.n, cfg.h_q, cfg.h_k, cfg.d, block, topk, dev["q"].dtype)
+    assert nsa.cmp_workspace_size(dims, L_K, STRIDE, max(seqlens)) > 0
+    kc, vc, cu_cmp = nsa.compress_kv(dev["k"], dev["v"], dev["cu"], L_K, STRIDE)
+    args = (dev["q"], kc, vc, dev["cu"], cu_cmp, L_K, STRIDE, max(seqlens), cfg.scale, block,
+            topk, init, local)
+    out_w, lse_w, sel_w = nsa.cmp_attn_select(*args)
+    out_s, lse_s, sel_s = nsa.cmp_attn_select(*args, use_workspace=False)
+    torch.cuda.synchronize()
+    assert torch.equal(sel_w, sel_s)
+    assert torch.equal(out_w, out_s)
+    assert torch.equal(torch.nan_to_num(lse_w), torch.nan_to_num(lse_s))
+    rng = np.random.default_rng(5)
+    toks = sorted(set(rng.integers(0, cfg.n, 120).tolist()) | {0, 31, 39999, 40000, 40299,
+                                                                 40300, cfg.n - 1})
+    rk, rv = oc.compress_kv(inp["cu_seqlens"], _f64(inp["k"]), _f64(inp["v"]), L_K, STRIDE)
+    rk, rv = _round16(rk, "bf16"), _round16(rv, "bf16")
+    ref_sel, imps, ref_out, ref_lse = oc.select_rows(inp["cu_seqlens"], _f64(inp["q"]), rk, rv,
+                                                     L_K, STRIDE, cfg.scale, block, topk, init,
+                                                     local, toks)
+    check_forward(out_w[toks], lse_w[:, toks], ref_out, ref_lse.T, "cmp workspace")
+    cu = inp["cu_seqlens"]
+    taus = [t - int(cu[np.searchsorted(cu, t, side="right") - 1]) for t in toks]
+    _check_selection(sel_w[:, toks].cpu().numpy(), ref_sel, imps, taus, block, topk, init,
+                     local, "workspace")
