@@ -506,6 +506,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 5) tmem_dealloc(tmem_base, L::kTmemCols);
 }
 
+// Partial rows each lane keeps in flight in the merge.
+#ifndef NSA_MERGE_BATCH
+#define NSA_MERGE_BATCH 16
+#endif
+
 // One warp per (token, query head): combine the <= T partials.
 template <int D, bool kFp16>
 __global__ void __launch_bounds__(256) fwd_merge_kernel(Params p) {
@@ -520,9 +525,11 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(Params p) {
     const int32_t pr = p.prow[((int64_t)h * p.n + t) * p.topk + lane];
     if (pr >= 0) row = (int64_t)pr + j;
   }
-  // The partial rows are loaded first, sixteen at a time, so that their latency
-  // overlaps the (m, l) load and the reductions of the weights.
-  constexpr int kBatch = 16;
+  // The weights come first (the (m, l) loads and their reductions), then the partial
+  // rows, kBatch at a time: with no loaded rows held across the reductions the kernel
+  // needs 32 registers, so twice as many warps keep loads in flight as when the rows
+  // were loaded first.
+  constexpr int kBatch = NSA_MERGE_BATCH;
   const uint16_t *obuf = static_cast<const uint16_t *>(p.obuf);
   auto load_rows = [&](int k0, uint32_t (&u)[kBatch][E / 2]) {
 #pragma unroll
@@ -543,7 +550,6 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(Params p) {
     }
   };
   uint32_t u[kBatch][E / 2];
-  load_rows(0, u);
   float2 ml = make_float2(-INFINITY, 0.f);
   if (row >= 0) ml = p.mlbuf[row];
   float M = ml.x;
@@ -558,7 +564,7 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(Params p) {
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   for (int k0 = 0; k0 < p.topk; k0 += kBatch) {
-    if (k0 > 0) load_rows(k0, u);
+    load_rows(k0, u);
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const float wk = __shfl_sync(0xffffffffu, w, (k0 + b) & 31);   // 0 for empty slots
