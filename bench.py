@@ -33,9 +33,9 @@ DOMINANT = ("fwd_main", "bwd_main")
 # kernels on the 64K workload, from one ncu capture of the kernel sources whose
 # SHA-256 is given (profiles/dram_traffic_fwd64k_g4.md).  Reported only while the
 # sources are unchanged; otherwise the roofline's traffic is null.
-TRAFFIC = {"sources_sha256": "87a067ecf4360de5264f173ed906895dcefa0d9414666f4f7cabb0b219484bd9",
-           "bytes": {"fwd_main": {"4": 927921408 + 4402221056},
-                     "bwd_main": {"4": 2872249856 + 4798644224}}}
+TRAFFIC = {"sources_sha256": "a3fded1d5a79fbe509a33ae2e9196e6d9f2b75e216b583d0eceebc1681db37a4",
+           "bytes": {"fwd_main": {"4": 925600000 + 4403003392},
+                     "bwd_main": {"4": 2803539200 + 4798355456}}}
 
 
 def kernel_sources_hash() -> str:
